@@ -5,15 +5,12 @@ The compute runs in the CUDA library ``libbl.so`` (C ABI, see include/bl.h).
 package does not load the library, so the input generators in ``synth`` can be
 used on machines without a GPU.
 """
+import importlib
 
-__all__ = ["binding", "synth"]
+__all__ = ["binding", "synth", "build"]
 
 
 def __getattr__(name):
-    if name == "binding":
-        from . import binding
-        return binding
-    if name == "synth":
-        from . import synth
-        return synth
+    if name in __all__:
+        return importlib.import_module(__name__ + "." + name)
     raise AttributeError(name)

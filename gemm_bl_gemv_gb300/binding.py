@@ -1,0 +1,222 @@
+"""Thin Python binding of libbl (include/bl.h) for torch CUDA tensors.
+
+Argument marshalling only: every function checks tensor dtypes/devices,
+allocates outputs with torch when none are given, and calls the C entry
+point of the same name on the current CUDA stream.  All computation happens
+in the library's kernels; there is no fallback.  A missing libbl.so raises
+ImportError (build it with gemm_bl_gemv_gb300.build.build()).
+"""
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libbl.so")
+
+BL_OK, BL_ERR_NULL, BL_ERR_SHAPE, BL_ERR_ALIGN, BL_ERR_DTYPE, BL_ERR_UNSUPPORTED, BL_ERR_CUDA = range(7)
+BL_F32, BL_BF16 = 0, 1
+BL_DEVERR_WAIT_TIMEOUT = 0x1
+
+EXPORTS = [
+    "bl_status_string", "bl_last_error", "bl_device_error", "bl_set_overlap", "bl_get_overlap",
+    "bl_pack_i2s", "bl_pack_tq2_0", "bl_pack_w1", "bl_quantize_act_absmax_int8",
+    "bl_gemv_i2s", "bl_gemv_tq2_0", "bl_gemm_w1a8", "bl_gemm_i2s_int8",
+]
+
+
+class BLError(RuntimeError):
+    def __init__(self, status, message):
+        super().__init__("%s: %s" % (status_name(status), message))
+        self.status = status
+
+
+def _declare(L):
+    p, i64, i32, st = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_int
+    sig = {
+        "bl_status_string": ([st], ctypes.c_char_p),
+        "bl_last_error": ([], ctypes.c_char_p),
+        "bl_device_error": ([p, i32], st),
+        "bl_set_overlap": ([i32], None),
+        "bl_get_overlap": ([], i32),
+        "bl_pack_i2s": ([p, ctypes.c_float, i64, i64, p, p], st),
+        "bl_pack_tq2_0": ([p, p, i64, i64, p, p], st),
+        "bl_pack_w1": ([p, i64, i64, p, p], st),
+        "bl_quantize_act_absmax_int8": ([p, i32, i64, i64, p, p, p], st),
+        "bl_gemv_i2s": ([p, p, i32, p, i32, i64, i64, p], st),
+        "bl_gemv_tq2_0": ([p, p, i32, p, i64, i64, p], st),
+        "bl_gemm_w1a8": ([p, p, p, p, p, i64, i64, i64, i32, p, p, p], st),
+        "bl_gemm_i2s_int8": ([p, p, p, i64, i64, i64, p, p, p], st),
+    }
+    for name, (args, res) in sig.items():
+        f = getattr(L, name)
+        f.argtypes = args
+        f.restype = res
+    return L
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError("libbl.so not built at %s; run gemm_bl_gemv_gb300.build.build()" % LIB_PATH)
+    return _declare(ctypes.CDLL(LIB_PATH))
+
+
+_lib = _load()
+
+
+def lib():
+    return _lib
+
+
+def status_name(s):
+    return _lib.bl_status_string(s).decode()
+
+
+def _check(status):
+    if status != BL_OK:
+        raise BLError(status, _lib.bl_last_error().decode())
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _dtype_code(t):
+    if t.dtype == torch.float32:
+        return BL_F32
+    if t.dtype == torch.bfloat16:
+        return BL_BF16
+    raise TypeError("unsupported dtype %s (float32 or bfloat16)" % t.dtype)
+
+
+def _cuda(t, name):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError("%s must be a CUDA tensor" % name)
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    return t
+
+
+def set_overlap(enable: bool):
+    _lib.bl_set_overlap(1 if enable else 0)
+
+
+def get_overlap() -> bool:
+    return bool(_lib.bl_get_overlap())
+
+
+def device_error(clear: bool = True) -> int:
+    v = ctypes.c_uint32(0)
+    _check(_lib.bl_device_error(ctypes.byref(v), 1 if clear else 0))
+    return v.value
+
+
+# ---- packing ---------------------------------------------------------------
+
+def i2s_packed_bytes(N, K):
+    return N * (K // 4) + 4
+
+
+def tq2_0_packed_bytes(N, K):
+    return N * (K // 256) * 66
+
+
+def bl_pack_i2s(w, scale, out=None, stream=None):
+    _cuda(w, "w")
+    N, K = w.shape
+    if out is None:
+        out = torch.empty(i2s_packed_bytes(N, K), dtype=torch.uint8, device=w.device)
+    _check(_lib.bl_pack_i2s(_ptr(w), ctypes.c_float(float(scale)), N, K, _ptr(_cuda(out, "out")), _stream(stream)))
+    return out
+
+
+def bl_pack_tq2_0(w, d_fp16_bits, out=None, stream=None):
+    _cuda(w, "w")
+    _cuda(d_fp16_bits, "d")
+    N, K = w.shape
+    if out is None:
+        out = torch.empty(tq2_0_packed_bytes(N, K), dtype=torch.uint8, device=w.device)
+    _check(_lib.bl_pack_tq2_0(_ptr(w), _ptr(d_fp16_bits), N, K, _ptr(_cuda(out, "out")), _stream(stream)))
+    return out
+
+
+def bl_pack_w1(w, out=None, stream=None):
+    _cuda(w, "w")
+    N, K = w.shape
+    if out is None:
+        out = torch.empty((N, K // 32), dtype=torch.int32, device=w.device)
+    _check(_lib.bl_pack_w1(_ptr(w), N, K, _ptr(_cuda(out, "out")), _stream(stream)))
+    return out
+
+
+# ---- activation quantization -------------------------------------------------
+
+def bl_quantize_act_absmax_int8(x, q=None, s=None, stream=None):
+    _cuda(x, "x")
+    M, K = x.shape
+    if q is None:
+        q = torch.empty((M, K), dtype=torch.int8, device=x.device)
+    if s is None:
+        s = torch.empty(M, dtype=torch.float32, device=x.device)
+    _check(_lib.bl_quantize_act_absmax_int8(_ptr(x), _dtype_code(x), M, K, _ptr(_cuda(q, "q")), _ptr(_cuda(s, "s")),
+                                            _stream(stream)))
+    return q, s
+
+
+# ---- products --------------------------------------------------------------
+
+def bl_gemv_i2s(packed, x, N, K, y=None, y_dtype=None, stream=None):
+    _cuda(packed, "packed")
+    _cuda(x, "x")
+    if y is None:
+        y = torch.empty(N, dtype=y_dtype or x.dtype, device=x.device)
+    _check(_lib.bl_gemv_i2s(_ptr(packed), _ptr(x), _dtype_code(x), _ptr(_cuda(y, "y")), _dtype_code(y), N, K,
+                            _stream(stream)))
+    return y
+
+
+def bl_gemv_tq2_0(packed, x, N, K, y=None, stream=None):
+    _cuda(packed, "packed")
+    _cuda(x, "x")
+    if y is None:
+        y = torch.empty(N, dtype=torch.float32, device=x.device)
+    _check(_lib.bl_gemv_tq2_0(_ptr(packed), _ptr(x), _dtype_code(x), _ptr(_cuda(y, "y")), N, K, _stream(stream)))
+    return y
+
+
+def bl_gemm_w1a8(q, s, wq, ws_fp16_bits, bias_bf16_bits=None, group=128, y=None, group_dots=False, stream=None):
+    for t, n in ((q, "q"), (s, "s"), (wq, "wq"), (ws_fp16_bits, "ws")):
+        _cuda(t, n)
+    M, K = q.shape
+    N = wq.shape[0]
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=q.device)
+    dots = None
+    if group_dots is True:
+        dots = torch.empty((M, N, K // group), dtype=torch.int32, device=q.device)
+    elif isinstance(group_dots, torch.Tensor):
+        dots = group_dots
+    _check(_lib.bl_gemm_w1a8(_ptr(q), _ptr(s), _ptr(wq), _ptr(ws_fp16_bits), _ptr(bias_bf16_bits), M, N, K, group,
+                             _ptr(_cuda(y, "y")), _ptr(dots), _stream(stream)))
+    return (y, dots) if dots is not None else y
+
+
+def bl_gemm_i2s_int8(q, s, packed, N, y=None, acc=False, stream=None):
+    for t, n in ((q, "q"), (s, "s"), (packed, "packed")):
+        _cuda(t, n)
+    M, K = q.shape
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float32, device=q.device)
+    a = None
+    if acc is True:
+        a = torch.empty((M, N), dtype=torch.int32, device=q.device)
+    elif isinstance(acc, torch.Tensor):
+        a = acc
+    _check(_lib.bl_gemm_i2s_int8(_ptr(q), _ptr(s), _ptr(packed), M, N, K, _ptr(_cuda(y, "y")), _ptr(a),
+                                 _stream(stream)))
+    return (y, a) if a is not None else y

@@ -1,0 +1,200 @@
+// C ABI of libbl: argument checks (before any launch), status codes, the
+// device error word and the overlap switch.  Every product and conversion is
+// done by the kernels in the other translation units.
+#include <atomic>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "bl.h"
+#include "bl_internal.h"
+
+namespace bl {
+
+// The library's device error word (BL_DEVERR_* bits).
+__device__ unsigned int g_dev_error = 0;
+
+namespace {
+std::atomic<int> g_overlap{0};
+thread_local char g_msg[512] = "";
+
+bl_status fail(bl_status st, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
+bl_status fail(bl_status st, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_msg, sizeof(g_msg), fmt, ap);
+  va_end(ap);
+  return st;
+}
+
+bl_status cuda_status(cudaError_t e, const char* what) {
+  if (e == cudaSuccess) return BL_OK;
+  return fail(BL_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+cudaStream_t S(bl_stream_t s) { return reinterpret_cast<cudaStream_t>(s); }
+}  // namespace
+
+bool overlap_enabled() { return g_overlap.load(std::memory_order_relaxed) != 0; }
+
+unsigned int* dev_error_ptr() {
+  static unsigned int* cache[64] = {nullptr};
+  static std::mutex mu;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!cache[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_dev_error) == cudaSuccess) cache[dev] = static_cast<unsigned int*>(p);
+  }
+  return cache[dev];
+}
+
+int sm_count() {
+  static int cache[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) dev = 0;
+  if (cache[dev] == 0) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    cache[dev] = n > 0 ? n : 1;
+  }
+  return cache[dev];
+}
+
+}  // namespace bl
+
+using namespace bl;
+
+extern "C" {
+
+const char* bl_status_string(bl_status s) {
+  switch (s) {
+    case BL_OK: return "BL_OK";
+    case BL_ERR_NULL: return "BL_ERR_NULL";
+    case BL_ERR_SHAPE: return "BL_ERR_SHAPE";
+    case BL_ERR_ALIGN: return "BL_ERR_ALIGN";
+    case BL_ERR_DTYPE: return "BL_ERR_DTYPE";
+    case BL_ERR_UNSUPPORTED: return "BL_ERR_UNSUPPORTED";
+    case BL_ERR_CUDA: return "BL_ERR_CUDA";
+  }
+  return "BL_UNKNOWN_STATUS";
+}
+
+const char* bl_last_error(void) { return g_msg; }
+
+bl_status bl_device_error(uint32_t* flags, int clear) {
+  if (!flags) return fail(BL_ERR_NULL, "bl_device_error: flags is NULL");
+  unsigned int v = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&v, bl::g_dev_error, sizeof(v));
+  if (e != cudaSuccess) return cuda_status(e, "bl_device_error read");
+  *flags = v;
+  if (clear) {
+    const unsigned int z = 0;
+    e = cudaMemcpyToSymbol(bl::g_dev_error, &z, sizeof(z));
+    if (e != cudaSuccess) return cuda_status(e, "bl_device_error clear");
+  }
+  return BL_OK;
+}
+
+void bl_set_overlap(int enable) { g_overlap.store(enable ? 1 : 0); }
+int bl_get_overlap(void) { return g_overlap.load(); }
+
+bl_status bl_pack_i2s(const int8_t* w, float scale, int64_t N, int64_t K, uint8_t* out, bl_stream_t stream) {
+  if (!w || !out) return fail(BL_ERR_NULL, "bl_pack_i2s: NULL pointer");
+  if (N < 1 || K < 128 || K % 128) return fail(BL_ERR_SHAPE, "bl_pack_i2s: need N >= 1, K %% 128 == 0 (N=%lld K=%lld)",
+                                               (long long)N, (long long)K);
+  if (!aligned(out, 16)) return fail(BL_ERR_ALIGN, "bl_pack_i2s: out must be 16-byte aligned");
+  return cuda_status(launch_pack_i2s(w, scale, N, K, out, S(stream)), "bl_pack_i2s");
+}
+
+bl_status bl_pack_tq2_0(const int8_t* w, const uint16_t* d_fp16, int64_t N, int64_t K, uint8_t* out,
+                        bl_stream_t stream) {
+  if (!w || !d_fp16 || !out) return fail(BL_ERR_NULL, "bl_pack_tq2_0: NULL pointer");
+  if (N < 1 || K < 256 || K % 256)
+    return fail(BL_ERR_SHAPE, "bl_pack_tq2_0: need N >= 1, K %% 256 == 0 (N=%lld K=%lld)", (long long)N, (long long)K);
+  if (!aligned(out, 2) || !aligned(d_fp16, 2)) return fail(BL_ERR_ALIGN, "bl_pack_tq2_0: out and d must be 2-byte aligned");
+  return cuda_status(launch_pack_tq2_0(w, d_fp16, N, K, out, S(stream)), "bl_pack_tq2_0");
+}
+
+bl_status bl_pack_w1(const int8_t* w, int64_t N, int64_t K, int32_t* out, bl_stream_t stream) {
+  if (!w || !out) return fail(BL_ERR_NULL, "bl_pack_w1: NULL pointer");
+  if (N < 1 || K < 32 || K % 32)
+    return fail(BL_ERR_SHAPE, "bl_pack_w1: need N >= 1, K %% 32 == 0 (N=%lld K=%lld)", (long long)N, (long long)K);
+  if (!aligned(out, 4)) return fail(BL_ERR_ALIGN, "bl_pack_w1: out must be 4-byte aligned");
+  return cuda_status(launch_pack_w1(w, N, K, out, S(stream)), "bl_pack_w1");
+}
+
+bl_status bl_quantize_act_absmax_int8(const void* x, bl_dtype xt, int64_t M, int64_t K, int8_t* q, float* s,
+                                      bl_stream_t stream) {
+  if (!x || !q || !s) return fail(BL_ERR_NULL, "bl_quantize_act_absmax_int8: NULL pointer");
+  if (xt != BL_F32 && xt != BL_BF16) return fail(BL_ERR_DTYPE, "bl_quantize_act_absmax_int8: bad dtype %d", int(xt));
+  if (M < 1 || K < 1 || M > 0x7fffffff)
+    return fail(BL_ERR_SHAPE, "bl_quantize_act_absmax_int8: need M >= 1, K >= 1 (M=%lld K=%lld)", (long long)M,
+                (long long)K);
+  if (!aligned(x, xt == BL_F32 ? 4 : 2) || !aligned(s, 4))
+    return fail(BL_ERR_ALIGN, "bl_quantize_act_absmax_int8: x and s must be aligned to their element size");
+  return cuda_status(launch_act_quant(x, xt, M, K, q, s, S(stream)), "bl_quantize_act_absmax_int8");
+}
+
+bl_status bl_gemv_i2s(const uint8_t* packed, const void* x, bl_dtype xt, void* y, bl_dtype yt, int64_t N, int64_t K,
+                      bl_stream_t stream) {
+  if (!packed || !x || !y) return fail(BL_ERR_NULL, "bl_gemv_i2s: NULL pointer");
+  if ((xt != BL_F32 && xt != BL_BF16) || (yt != BL_F32 && yt != BL_BF16))
+    return fail(BL_ERR_DTYPE, "bl_gemv_i2s: bad dtype (x %d, y %d)", int(xt), int(yt));
+  if (N < 1 || K < 128 || K % 128 || N > 0x7fffffff)
+    return fail(BL_ERR_SHAPE, "bl_gemv_i2s: need N >= 1, K %% 128 == 0 (N=%lld K=%lld)", (long long)N, (long long)K);
+  if (K / 128 > 1024) return fail(BL_ERR_UNSUPPORTED, "bl_gemv_i2s: K up to 131072 supported (K=%lld)", (long long)K);
+  if (!aligned(packed, 16)) return fail(BL_ERR_ALIGN, "bl_gemv_i2s: packed must be 16-byte aligned");
+  if (!aligned(x, xt == BL_F32 ? 4 : 2) || !aligned(y, yt == BL_F32 ? 4 : 2))
+    return fail(BL_ERR_ALIGN, "bl_gemv_i2s: x and y must be aligned to their element size");
+  return cuda_status(launch_gemv_i2s(packed, x, xt, y, yt, N, K, S(stream)), "bl_gemv_i2s");
+}
+
+bl_status bl_gemv_tq2_0(const uint8_t* packed, const void* x, bl_dtype xt, float* y, int64_t N, int64_t K,
+                        bl_stream_t stream) {
+  if (!packed || !x || !y) return fail(BL_ERR_NULL, "bl_gemv_tq2_0: NULL pointer");
+  if (xt != BL_F32 && xt != BL_BF16) return fail(BL_ERR_DTYPE, "bl_gemv_tq2_0: bad dtype %d", int(xt));
+  if (N < 1 || K < 256 || K % 256 || N > 0x7fffffff)
+    return fail(BL_ERR_SHAPE, "bl_gemv_tq2_0: need N >= 1, K %% 256 == 0 (N=%lld K=%lld)", (long long)N, (long long)K);
+  if (K / 256 > 1024) return fail(BL_ERR_UNSUPPORTED, "bl_gemv_tq2_0: K up to 262144 supported (K=%lld)", (long long)K);
+  if (!aligned(packed, 16)) return fail(BL_ERR_ALIGN, "bl_gemv_tq2_0: packed must be 16-byte aligned");
+  if (!aligned(x, xt == BL_F32 ? 4 : 2) || !aligned(y, 4))
+    return fail(BL_ERR_ALIGN, "bl_gemv_tq2_0: x and y must be aligned to their element size");
+  return cuda_status(launch_gemv_tq2_0(packed, x, xt, y, N, K, S(stream)), "bl_gemv_tq2_0");
+}
+
+bl_status bl_gemm_w1a8(const int8_t* q, const float* s, const int32_t* wq, const uint16_t* ws_fp16,
+                       const uint16_t* bias_bf16, int64_t M, int64_t N, int64_t K, int group, uint16_t* y_bf16,
+                       int32_t* group_dots, bl_stream_t stream) {
+  if (!q || !s || !wq || !ws_fp16 || !y_bf16) return fail(BL_ERR_NULL, "bl_gemm_w1a8: NULL pointer");
+  if (M < 1 || M > 8) return fail(BL_ERR_UNSUPPORTED, "bl_gemm_w1a8: 1 <= M <= 8 supported (M=%lld)", (long long)M);
+  if (N < 1 || K < 32 || K % 32 || group < 32 || group % 32 || K % group || N > 0x7fffffff)
+    return fail(BL_ERR_SHAPE, "bl_gemm_w1a8: need N >= 1, K %% 32 == 0, group %% 32 == 0, K %% group == 0 "
+                "(N=%lld K=%lld group=%d)", (long long)N, (long long)K, group);
+  if (K / group > 1024) return fail(BL_ERR_UNSUPPORTED, "bl_gemm_w1a8: at most 1024 groups per row");
+  if (!aligned(q, 16) || !aligned(wq, 16) || !aligned(ws_fp16, 16) || !aligned(s, 4) || !aligned(y_bf16, 2) ||
+      (bias_bf16 && !aligned(bias_bf16, 2)) || (group_dots && !aligned(group_dots, 4)))
+    return fail(BL_ERR_ALIGN, "bl_gemm_w1a8: q, wq, ws must be 16-byte aligned; others to their element size");
+  return cuda_status(launch_gemm_w1a8(q, s, wq, ws_fp16, bias_bf16, M, N, K, group, y_bf16, group_dots, S(stream)),
+                     "bl_gemm_w1a8");
+}
+
+bl_status bl_gemm_i2s_int8(const int8_t* q, const float* s, const uint8_t* packed, int64_t M, int64_t N, int64_t K,
+                           float* y, int32_t* acc, bl_stream_t stream) {
+  if (!q || !s || !packed || !y) return fail(BL_ERR_NULL, "bl_gemm_i2s_int8: NULL pointer");
+  if (M < 1 || N < 1 || K < 128 || K % 128 || N > 0x7fffffff || M > 0x7fffffff)
+    return fail(BL_ERR_SHAPE, "bl_gemm_i2s_int8: need M, N >= 1, K %% 128 == 0 (M=%lld N=%lld K=%lld)", (long long)M,
+                (long long)N, (long long)K);
+  if (K > 132096) return fail(BL_ERR_UNSUPPORTED, "bl_gemm_i2s_int8: K <= 132096 supported (K=%lld)", (long long)K);
+  if (!aligned(q, 16) || !aligned(s, 16) || !aligned(packed, 16) || !aligned(y, 16) || (acc && !aligned(acc, 16)))
+    return fail(BL_ERR_ALIGN, "bl_gemm_i2s_int8: all pointers must be 16-byte aligned");
+  return cuda_status(launch_gemm_i2s_int8(q, s, packed, M, N, K, y, acc, S(stream)), "bl_gemm_i2s_int8");
+}
+
+}  // extern "C"

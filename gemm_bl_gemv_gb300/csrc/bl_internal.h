@@ -1,0 +1,56 @@
+// Host-side internals of libbl: launch functions called by the C ABI layer.
+#pragma once
+#include <cstdint>
+#include <utility>
+#include <cuda_runtime.h>
+
+#include "bl.h"
+
+namespace bl {
+
+// Overlap (programmatic dependent launch) setting, see bl_set_overlap().
+bool overlap_enabled();
+
+// Number of SMs of the current device (cached per device).
+int sm_count();
+
+// Device address of the library's error word on the current device (the
+// BL_DEVERR_* bits read by bl_device_error()); kernels receive it as an
+// argument.  nullptr if it cannot be resolved.
+unsigned int* dev_error_ptr();
+
+// Launch helper: cudaLaunchKernelEx with the PDL attribute when overlap is on.
+template <typename... KArgs, typename... Args>
+cudaError_t launch(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream, bool pdl,
+                   Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+// ---- launchers (validated arguments only) --------------------------------
+cudaError_t launch_pack_i2s(const int8_t* w, float scale, int64_t N, int64_t K, uint8_t* out, cudaStream_t s);
+cudaError_t launch_pack_tq2_0(const int8_t* w, const uint16_t* d, int64_t N, int64_t K, uint8_t* out, cudaStream_t s);
+cudaError_t launch_pack_w1(const int8_t* w, int64_t N, int64_t K, int32_t* out, cudaStream_t s);
+cudaError_t launch_act_quant(const void* x, bl_dtype xt, int64_t M, int64_t K, int8_t* q, float* sc, cudaStream_t s);
+cudaError_t launch_gemv_i2s(const uint8_t* packed, const void* x, bl_dtype xt, void* y, bl_dtype yt, int64_t N,
+                            int64_t K, cudaStream_t s);
+cudaError_t launch_gemv_tq2_0(const uint8_t* packed, const void* x, bl_dtype xt, float* y, int64_t N, int64_t K,
+                              cudaStream_t s);
+cudaError_t launch_gemm_w1a8(const int8_t* q, const float* sc, const int32_t* wq, const uint16_t* ws,
+                             const uint16_t* bias, int64_t M, int64_t N, int64_t K, int group, uint16_t* y,
+                             int32_t* dots, cudaStream_t s);
+cudaError_t launch_gemm_i2s_int8_simt(const int8_t* q, const float* sc, const uint8_t* packed, int64_t M, int64_t N,
+                                      int64_t K, float* y, int32_t* acc, cudaStream_t s);
+cudaError_t launch_gemm_i2s_int8(const int8_t* q, const float* sc, const uint8_t* packed, int64_t M, int64_t N,
+                                 int64_t K, float* y, int32_t* acc, cudaStream_t s);
+
+}  // namespace bl

@@ -1,0 +1,228 @@
+/*
+ * bl.h -- C ABI of libbl, packed BitLinear products on NVIDIA GB300 (sm_103a).
+ *
+ * The library computes the BitLinear product y = scale * W x where W is
+ * ternary {-1,0,+1} or binary {-1,+1} and stays packed in memory; weights are
+ * decoded in registers inside the kernels and never written out.
+ *
+ * Conventions shared by every entry point
+ * ----------------------------------------
+ *  - All tensor pointers are DEVICE pointers owned by the caller.  The library
+ *    allocates no memory and keeps no per-call state.
+ *  - Every call is asynchronous: it only enqueues kernels on `stream` (a
+ *    cudaStream_t / CUstream handle passed as void*, NULL = legacy default
+ *    stream) and returns.  Nothing inside a call synchronizes with the host.
+ *  - Arguments are checked on the host BEFORE any launch; a failed check
+ *    returns a status and launches nothing.  A launch failure returns
+ *    BL_ERR_CUDA.  bl_last_error() gives a message for the calling thread.
+ *  - Row-major layouts throughout.  bf16 and fp16 values are passed as their
+ *    16-bit patterns (uint16_t); int32 words and fp32 scales are
+ *    little-endian as in device memory.
+ *  - Results are deterministic: repeated calls with the same inputs give
+ *    bitwise identical outputs (fixed reduction order, no atomics on data).
+ *  - Kernels never spin without bound.  A pipeline wait that exceeds its
+ *    time limit (about one second) makes the kernel record a flag in the
+ *    library's device error word and return; bl_device_error() reads it.
+ *
+ * Passages referred to below (page title, section):
+ *  [BL]  "Hesper/Layers/BitLinear": "i2_s Packing Format", "BitLinear
+ *        Mathematics", "High-Level API".
+ *  [TQ]  "Hesper/Quantization/TQ2_0": "TQ2_0 Format", "Memory Layout Example".
+ *  [BG]  "binary-gemm" card: "API", "Method", "Correctness",
+ *        "Requirements and limits".
+ */
+#ifndef BL_H
+#define BL_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  BL_OK = 0,
+  BL_ERR_NULL = 1,         /* a required pointer is NULL                      */
+  BL_ERR_SHAPE = 2,        /* a size is negative, zero where not allowed, or
+                              not a multiple the format requires              */
+  BL_ERR_ALIGN = 3,        /* a pointer is not aligned as documented          */
+  BL_ERR_DTYPE = 4,        /* an unsupported bl_dtype value                   */
+  BL_ERR_UNSUPPORTED = 5,  /* valid request outside what this build supports  */
+  BL_ERR_CUDA = 6          /* the CUDA runtime reported an error              */
+} bl_status;
+
+typedef enum {
+  BL_F32 = 0,              /* IEEE binary32                                   */
+  BL_BF16 = 1              /* bfloat16, passed as uint16_t bit patterns        */
+} bl_dtype;
+
+typedef void* bl_stream_t; /* a cudaStream_t / CUstream handle                */
+
+/* Human-readable name of a status code (static string). */
+const char* bl_status_string(bl_status s);
+
+/* Message describing the last failed call on the calling host thread. */
+const char* bl_last_error(void);
+
+/*
+ * Read the library's device error word (synchronizes the device).
+ * *flags receives the OR of BL_DEVERR_* bits recorded since the last clear;
+ * clear != 0 resets it to zero.  Returns BL_ERR_CUDA if the read fails.
+ */
+#define BL_DEVERR_WAIT_TIMEOUT 0x1u   /* a pipeline wait exceeded its limit */
+bl_status bl_device_error(uint32_t* flags, int clear);
+
+/*
+ * Allow back-to-back launches to overlap (programmatic dependent launch).
+ * When enabled, the GEMV/GEMM kernels launched afterwards on any stream may
+ * start while the previous kernel on the same stream is still running: they
+ * fetch their PACKED WEIGHTS before waiting for that kernel, and wait for it
+ * before reading activations or writing outputs.  Enable it only when no
+ * kernel writes the weight buffers right before a product that reads them
+ * (weights written by bl_pack_* must be followed by a stream-ordered event
+ * or any other kernel first).  Default: disabled.  Process-wide setting.
+ */
+void bl_set_overlap(int enable);
+int bl_get_overlap(void);
+
+/* ------------------------------------------------------------------------ */
+/* Packing (load time).                                                       */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * i2_s packing [BL "i2_s Packing Format"].
+ *   w     : int8 [N, K] ternary values, row-major.  Values > 0 store +1,
+ *           < 0 store -1, 0 stores 0 (code 0b11 is never produced).
+ *   scale : the tensor's fp32 scale, stored after the codes.
+ *   out   : uint8 [N*K/4 + 4].  Row n occupies bytes [n*K/4, (n+1)*K/4);
+ *           element e of a row sits in byte (e/128)*32 + e%32 at bits
+ *           (7-2t):(6-2t) with t = (e%128)/32; codes -1 -> 0b00, 0 -> 0b01,
+ *           +1 -> 0b10.  The 4 bytes after the last row hold `scale`
+ *           (little-endian).
+ * Requires K % 128 == 0, N >= 1; `out` 16-byte aligned.
+ */
+bl_status bl_pack_i2s(const int8_t* w, float scale, int64_t N, int64_t K, uint8_t* out, bl_stream_t stream);
+
+/*
+ * TQ2_0 packing [TQ "TQ2_0 Format", "Memory Layout Example"].
+ *   w      : int8 [N, K] ternary values (sign taken as for i2_s).
+ *   d_fp16 : fp16 bit patterns [N, K/256], one scale per 256-element block.
+ *   out    : uint8 [N * (K/256) * 66].  Blocks follow each other in K order
+ *            within a row, rows follow each other.  A block is 64 code bytes
+ *            then its fp16 scale (low byte first).  Element j of a block sits
+ *            in byte j/4 at bits (2*(j%4)+1):(2*(j%4)), codes 0 -> 0b00,
+ *            +1 -> 0b01, -1 -> 0b11 (0b10 is never produced).  The in-byte
+ *            order is this library's reading of the page, which prints the
+ *            code table and the 2*idx shift of its unpack helper but not the
+ *            element order.
+ * Requires K % 256 == 0, N >= 1; `out` 2-byte aligned.
+ */
+bl_status bl_pack_tq2_0(const int8_t* w, const uint16_t* d_fp16, int64_t N, int64_t K, uint8_t* out,
+                        bl_stream_t stream);
+
+/*
+ * W1 sign-bit packing [BG "API" pack_weights, "Method", "Correctness"].
+ *   w   : int8 [N, K]; values > 0 store bit 1 (+1), all others bit 0 (-1):
+ *         zeros pack as -1, as the card states.
+ *   out : int32 [N, K/32]; element k of a row sits at bit k%32 of word k/32
+ *         (lowest bit first; the bit order is this library's reading).
+ * Requires K % 32 == 0, N >= 1; `out` 4-byte aligned.
+ */
+bl_status bl_pack_w1(const int8_t* w, int64_t N, int64_t K, int32_t* out, bl_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Activation quantization.                                                   */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * Per-token absmax int8 quantization [BG "API" quantize_activation,
+ * "Correctness"].  For every row m of x [M, K] (fp32 or bf16), in binary32
+ * with round-to-nearest-even:
+ *   amax = max_k |x[m,k]|;  if amax == 0: q[m,:] = 0, s[m] = 0;
+ *   otherwise inv = 127/amax, q[m,k] = clamp(rint(x[m,k]*inv), -127, 127),
+ *   s[m] = amax/127.
+ * (The card states only "per-token absmax" with under 1% reconstruction
+ * error; this formula is the library's reading and meets that bound.)
+ *   q : int8 [M, K];  s : fp32 [M].
+ * Requires M >= 1, K >= 1.  x must be aligned to its element size.
+ * Non-finite inputs give unspecified q and s.
+ */
+bl_status bl_quantize_act_absmax_int8(const void* x, bl_dtype xt, int64_t M, int64_t K, int8_t* q, float* s,
+                                      bl_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Products.                                                                  */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * i2_s GEMV, one token [BL "BitLinear Mathematics": y[i] = scale *
+ * sum_j w[i,j] x[j]].
+ *   packed : the i2_s tensor as written by bl_pack_i2s (codes + trailing
+ *            fp32 scale, which the kernel reads from device memory).
+ *   x      : [K] fp32 (xt = BL_F32) or bf16 (xt = BL_BF16).
+ *   y      : [N] fp32 or bf16 (yt).  bf16 output is rounded to nearest even.
+ * Accuracy: within each 128-element group x is carried as a fixed-point
+ * integer of 30 bits (fp32 input) or 22 bits (bf16 input) relative to the
+ * group's max|x|: bf16 inputs within 14 binades of the group maximum and
+ * fp32 inputs within 6 binades are carried exactly, smaller values with an
+ * absolute error of at most 2^-31 (fp32) / 2^-23 (bf16) times the group
+ * maximum.  Products and sums inside a group are exact integers; each group
+ * sum is converted to fp32 once and the group sums are added in fp32, then
+ * rounded to bf16 if asked.  For activations without extreme in-group
+ * outliers the error is within 1e-5 (fp32 output) / 2e-2 (bf16 output) of
+ * |scale| * sum_j |w[i,j]| |x[j]| + |y[i]|.
+ * Requires K % 128 == 0, N >= 1; `packed` 16-byte aligned; x and y aligned
+ * to their element size.  Non-finite x gives unspecified y.
+ */
+bl_status bl_gemv_i2s(const uint8_t* packed, const void* x, bl_dtype xt, void* y, bl_dtype yt, int64_t N, int64_t K,
+                      bl_stream_t stream);
+
+/*
+ * TQ2_0 GEMV, one token [TQ "TQ2_0 Format"]:
+ *   y[n] = sum_b d[n,b] * sum_{j<256} w[n,256b+j] x[256b+j].
+ *   packed : as written by bl_pack_tq2_0.  x : [K] fp32 or bf16.  y : fp32 [N].
+ * Accuracy as for bl_gemv_i2s (fp32 output), with one fixed-point exponent
+ * per 256-element block.
+ * Requires K % 256 == 0, N >= 1; `packed` 16-byte aligned.
+ */
+bl_status bl_gemv_tq2_0(const uint8_t* packed, const void* x, bl_dtype xt, float* y, int64_t N, int64_t K,
+                        bl_stream_t stream);
+
+/*
+ * W1A8 product for small batches [BG "API" binary_gemm, "Method"]:
+ *   dot[m,n,g] = sum_{k in group g} w[n,k] q[m,k]              (exact int32)
+ *   y[m,n]     = bf16( s[m] * sum_g f32(ws[n,g]) * dot[m,n,g] + bias[n] )
+ *   q        : int8 [M, K] activations; s : fp32 [M] per-token scales.
+ *   wq       : int32 [N, K/32] as written by bl_pack_w1.
+ *   ws_fp16  : fp16 bit patterns [N, K/group].
+ *   bias_bf16: bf16 bit patterns [N], or NULL for no bias.
+ *   y_bf16   : bf16 bit patterns [M, N].
+ *   group_dots: int32 [M, N, K/group] or NULL; when given, the exact group
+ *              dot products are written too (a separate, slower kernel
+ *              variant meant for verification).
+ * The fp32 sum over groups runs in an order of the library's choosing.
+ * Requires 1 <= M <= 8, K % 32 == 0, group % 32 == 0, K % group == 0,
+ * N >= 1; wq 16-byte aligned.
+ */
+bl_status bl_gemm_w1a8(const int8_t* q, const float* s, const int32_t* wq, const uint16_t* ws_fp16,
+                       const uint16_t* bias_bf16, int64_t M, int64_t N, int64_t K, int group, uint16_t* y_bf16,
+                       int32_t* group_dots, bl_stream_t stream);
+
+/*
+ * i2_s product with int8 activations (prefill, large M)
+ * [BL "BitLinear Mathematics"; activations as BG "quantize_activation"]:
+ *   acc[m,n] = sum_k q[m,k] w[n,k]          (exact int32)
+ *   y[m,n]   = f32(acc[m,n]) * s[m] * scale  (scale: the i2_s tensor scale)
+ *   q : int8 [M, K];  s : fp32 [M];  packed : i2_s tensor (bl_pack_i2s).
+ *   y : fp32 [M, N];  acc : int32 [M, N] or NULL (when given, also written).
+ * Requires M >= 1, N >= 1, K % 128 == 0, K <= 132096 (so that every
+ * accumulator stays exactly representable); all pointers 16-byte aligned.
+ */
+bl_status bl_gemm_i2s_int8(const int8_t* q, const float* s, const uint8_t* packed, int64_t M, int64_t N, int64_t K,
+                           float* y, int32_t* acc, bl_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BL_H */

@@ -1,0 +1,350 @@
+"""GPU path (libbl through its C ABI) against the CPU oracle, element by element.
+
+Integer and byte results (packed bytes, int8 activations, int32 group dots and
+accumulators) must be bit-exact; floating-point results must meet the
+tolerance in tests/parity.py.  Shapes span several tiles and a ragged tail;
+the full-size workloads are checked on sampled rows, in the launch
+configuration the benchmark times.
+"""
+import numpy as np
+import pytest
+import torch
+
+from gemm_bl_gemv_gb300 import synth
+from oracle import oracle as O
+from parity import TOL_BF16, TOL_F32, assert_close, bf16_gpu, bits16, fp16_gpu, to_gpu, x_f64
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def B():
+    from gemm_bl_gemv_gb300 import build
+    build.build()
+    from gemm_bl_gemv_gb300 import binding
+    binding.set_overlap(False)
+    binding.device_error(clear=True)
+    yield binding
+    torch.cuda.synchronize()
+    assert binding.device_error(clear=True) == 0, "a kernel recorded a device-side wait timeout"
+
+
+def rng(seed):
+    return np.random.Generator(np.random.PCG64(seed))
+
+
+def ternary(g, N, K, p0=1 / 3):
+    return synth.ternary(g, (N, K), p0)
+
+
+def rand_x(g, K, dtype, M=None):
+    shape = (K,) if M is None else (M, K)
+    x = synth.normal_f32(g, shape)
+    return x if dtype == "f32" else synth.f32_to_bf16_bits(x)
+
+
+def x_gpu(x, dtype):
+    return to_gpu(x) if dtype == "f32" else bf16_gpu(x)
+
+
+# ---------------------------------------------------------------------------
+# packing: bit-exact
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("N,K", [(1, 128), (7, 256), (33, 2560), (64, 6912)])
+def test_pack_i2s_bit_exact(B, N, K):
+    g = rng(N * 1000 + K)
+    w = ternary(g, N, K)
+    w[0, :] = 0
+    if N > 2:
+        w[1, :] = 1
+        w[2, :] = -1
+    got = B.bl_pack_i2s(to_gpu(w), 1.5).cpu().numpy()
+    assert np.array_equal(got, O.pack_i2s(w, np.float32(1.5)))
+
+
+@pytest.mark.parametrize("N,K", [(1, 256), (5, 512), (33, 5120)])
+def test_pack_tq2_0_bit_exact(B, N, K):
+    g = rng(N * 7 + K)
+    w = ternary(g, N, K)
+    d = synth.abs_normal_fp16_bits(g, (N, K // 256), 0.02)
+    got = B.bl_pack_tq2_0(to_gpu(w), fp16_gpu(d)).cpu().numpy()
+    assert np.array_equal(got, O.pack_tq2_0(w, d))
+
+
+@pytest.mark.parametrize("N,K", [(1, 32), (3, 96), (17, 5120)])
+def test_pack_w1_bit_exact(B, N, K):
+    g = rng(N * 11 + K)
+    w = ternary(g, N, K)  # zeros must pack as -1
+    got = B.bl_pack_w1(to_gpu(w)).cpu().numpy()
+    assert np.array_equal(got, O.pack_w1(w))
+
+
+# ---------------------------------------------------------------------------
+# activation quantization: bit-exact q and s
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("M,K", [(1, 1), (3, 7), (8, 5120), (512, 2560), (2, 70000)])
+def test_act_quant_bit_exact(B, dtype, M, K):
+    g = rng(M * 31 + K)
+    x = synth.normal_f32(g, (M, K)) * g.uniform(0.01, 100, (M, 1)).astype(np.float32)
+    if M >= 3:
+        x[1] = 0.0                                    # zero row
+        x[2, : min(K, 4)] = [127.0, 0.5, 1.5, -2.5][: min(K, 4)]  # ties to even with amax 127
+        if K > 4:
+            x[2, 4:] = 0.0
+    xin = x if dtype == "f32" else synth.f32_to_bf16_bits(x)
+    q, s = B.bl_quantize_act_absmax_int8(x_gpu(xin, dtype))
+    qo, so = O.quantize_act_absmax_int8(xin, dtype)
+    assert np.array_equal(q.cpu().numpy(), qo)
+    assert np.array_equal(s.cpu().numpy().view(np.uint32), so.view(np.uint32))
+
+
+# ---------------------------------------------------------------------------
+# i2_s GEMV
+# ---------------------------------------------------------------------------
+
+def run_gemv_i2s(B, w, scale, x, xd, yd):
+    N, K = w.shape
+    packed = B.bl_pack_i2s(to_gpu(w), scale)
+    y = B.bl_gemv_i2s(packed, x_gpu(x, xd), N, K, y_dtype=torch.float32 if yd == "f32" else torch.bfloat16)
+    yv = y.cpu().numpy().astype(np.float64) if yd == "f32" else x_f64(bits16(y), "bf16")
+    ref, cond = O.gemv_i2s(O.pack_i2s(w, scale), x_f64(x, xd), N, K)
+    return yv, ref, cond
+
+
+@pytest.mark.parametrize("xd,yd", [("f32", "f32"), ("bf16", "bf16"), ("bf16", "f32"), ("f32", "bf16")])
+@pytest.mark.parametrize("N,K", [(1, 128), (3, 384), (31, 2560), (33, 2560), (100, 1024), (257, 6912)])
+def test_gemv_i2s_small(B, xd, yd, N, K):
+    g = rng(N + 13 * K)
+    w = ternary(g, N, K)
+    x = rand_x(g, K, xd)
+    scale = np.float32(g.uniform(0.5, 2.0))
+    y, ref, cond = run_gemv_i2s(B, w, scale, x, xd, yd)
+    assert_close(y, ref, cond, TOL_F32 if yd == "f32" else TOL_BF16, "gemv_i2s %dx%d %s->%s" % (N, K, xd, yd))
+
+
+def test_gemv_i2s_extreme_inputs(B):
+    """Degenerate activations: all zero, a 1e4 outlier in one group, tiny
+    values (1e-30), all equal; and an all-zero weight row."""
+    K, N = 512, 40
+    g = rng(5)
+    w = ternary(g, N, K)
+    w[0] = 0
+    base = synth.normal_f32(g, (K,))
+    outlier = base.copy()
+    outlier[7] = 1e4
+    for x in [np.zeros(K, np.float32), outlier, (base * 1e-30).astype(np.float32), np.full(K, -1.0, np.float32)]:
+        for xd, yd in (("f32", "f32"), ("bf16", "bf16")):
+            xx = x if xd == "f32" else synth.f32_to_bf16_bits(x)
+            y, ref, cond = run_gemv_i2s(B, w, np.float32(1.25), xx, xd, yd)
+            assert_close(y, ref, cond, TOL_F32 if yd == "f32" else TOL_BF16, "gemv_i2s extreme")
+
+
+def test_gemv_i2s_workload_2560(B):
+    """i2_s GEMV 2560x2560, fp32 in/out (all rows)."""
+    wl = synth.WORKLOADS["i2s_gemv_2560"]
+    w = synth.weight_matrix(wl.index, "w", wl.N, wl.K, "ternary", wl.p_zero)
+    x = synth.activations(wl.index, 1, wl.K, "f32")[0]
+    y, ref, cond = run_gemv_i2s(B, w, synth.tensor_scale(wl.index), x, "f32", "f32")
+    assert_close(y, ref, cond, TOL_F32, "i2s_gemv_2560")
+
+
+@pytest.mark.parametrize("mat", ["gate", "up", "down"])
+def test_gemv_i2s_workload_mlp(B, mat):
+    """BitNet-2B MLP shapes, bf16 in/out (all rows)."""
+    wl = synth.WORKLOADS["i2s_mlp_bitnet2b"]
+    N, K = wl.extra[mat]
+    w = synth.weight_matrix(wl.index, "w_" + mat, N, K, "ternary", wl.p_zero)
+    x = synth.activations(wl.index, 1, K, "bf16", tensor="x" if mat != "down" else "x_down")[0]
+    y, ref, cond = run_gemv_i2s(B, w, synth.tensor_scale(wl.index, "scale_" + mat), x, "bf16", "bf16")
+    assert_close(y, ref, cond, TOL_BF16, "mlp " + mat)
+
+
+# ---------------------------------------------------------------------------
+# TQ2_0 GEMV
+# ---------------------------------------------------------------------------
+
+def run_gemv_tq2(B, w, d, x, xd):
+    N, K = w.shape
+    packed = B.bl_pack_tq2_0(to_gpu(w), fp16_gpu(d))
+    y = B.bl_gemv_tq2_0(packed, x_gpu(x, xd), N, K).cpu().numpy().astype(np.float64)
+    ref, cond = O.gemv_tq2_0(O.pack_tq2_0(w, d), x_f64(x, xd), N, K)
+    return y, ref, cond
+
+
+@pytest.mark.parametrize("xd", ["f32", "bf16"])
+@pytest.mark.parametrize("N,K", [(1, 256), (5, 512), (31, 5120), (33, 5120), (70, 1792), (130, 256)])
+def test_gemv_tq2_0_small(B, xd, N, K):
+    g = rng(3 * N + K)
+    w = ternary(g, N, K)
+    d = synth.abs_normal_fp16_bits(g, (N, K // 256), 0.02)
+    d[0, 0] = 0x0001          # an fp16 subnormal scale
+    x = rand_x(g, K, xd)
+    y, ref, cond = run_gemv_tq2(B, w, d, x, xd)
+    assert_close(y, ref, cond, TOL_F32, "gemv_tq2_0 %dx%d %s" % (N, K, xd))
+
+
+def test_gemv_tq2_0_workload(B):
+    wl = synth.WORKLOADS["tq2_0_gemv_5120x13824"]
+    w = synth.weight_matrix(wl.index, "w", wl.N, wl.K, "ternary", wl.p_zero)
+    d = synth.block_scale_matrix(wl.index, wl.N, wl.K // 256)
+    x = synth.activations(wl.index, 1, wl.K, "bf16")[0]
+    y, ref, cond = run_gemv_tq2(B, w, d, x, "bf16")
+    assert_close(y, ref, cond, TOL_F32, "tq2_0 workload")
+
+
+# ---------------------------------------------------------------------------
+# W1A8
+# ---------------------------------------------------------------------------
+
+def run_w1a8(B, w, ws, bias, q, s, G, rows=None, wq_gpu=None):
+    N, K = w.shape if w is not None else (wq_gpu.shape[0], wq_gpu.shape[1] * 32)
+    if wq_gpu is None:
+        wq_gpu = B.bl_pack_w1(to_gpu(w))
+    y, dots = B.bl_gemm_w1a8(to_gpu(q), to_gpu(s), wq_gpu, fp16_gpu(ws),
+                             None if bias is None else bf16_gpu(bias), group=G, group_dots=True)
+    yb = bits16(y)
+    dots = dots.cpu().numpy()
+    return yb, dots
+
+
+@pytest.mark.parametrize("M", [1, 2, 3, 4, 8])
+@pytest.mark.parametrize("G", [32, 64, 128, 256])
+@pytest.mark.parametrize("N,K", [(1, 256), (37, 512), (100, 5120)])
+def test_gemm_w1a8_small(B, M, G, N, K):
+    if K % G:
+        pytest.skip("K not a multiple of G")
+    g = rng(M * 100 + G + N + K)
+    w = synth.signs(g, (N, K))
+    xb = rand_x(g, K, "bf16", M)
+    q, s = O.quantize_act_absmax_int8(xb, "bf16")
+    ws = synth.abs_normal_fp16_bits(g, (N, K // G), 0.02)
+    bias = synth.f32_to_bf16_bits(synth.normal_f32(g, (N,))) if (M + G) % 2 else None
+    yb, dots = run_w1a8(B, w, ws, bias, q, s, G)
+    wq = O.pack_w1(w)
+    dref, yref, cond = O.gemm_w1a8(q, s, wq, ws, bias, K, G)
+    assert np.array_equal(dots.astype(np.int64), dref), "group dots must be bit-exact"
+    assert_close(x_f64(yb, "bf16"), yref, cond, TOL_BF16, "w1a8 M=%d G=%d %dx%d" % (M, G, N, K))
+
+
+def test_gemm_w1a8_no_dots_matches_dots_variant(B):
+    g = rng(77)
+    M, N, K, G = 4, 300, 1024, 128
+    w = synth.signs(g, (N, K))
+    q, s = O.quantize_act_absmax_int8(rand_x(g, K, "bf16", M), "bf16")
+    ws = synth.abs_normal_fp16_bits(g, (N, K // G), 0.02)
+    wq = B.bl_pack_w1(to_gpu(w))
+    y1 = B.bl_gemm_w1a8(to_gpu(q), to_gpu(s), wq, fp16_gpu(ws), group=G)
+    y2, _ = B.bl_gemm_w1a8(to_gpu(q), to_gpu(s), wq, fp16_gpu(ws), group=G, group_dots=True)
+    assert torch.equal(y1.view(torch.int16), y2.view(torch.int16))
+
+
+@pytest.mark.parametrize("M", [1, 4, 8])
+def test_gemm_w1a8_workload_lmhead(B, M):
+    """LM head 5120 -> 248320, sampled rows, the benchmark's launch (no dot output)."""
+    wl = synth.WORKLOADS["w1a8_lmhead_248320"]
+    N, K, G = wl.N, wl.K, wl.group
+    wq = torch.empty((N, K // 32), dtype=torch.int32, device="cuda")
+    for b in range((N + synth.ROW_BLOCK - 1) // synth.ROW_BLOCK):
+        blk = synth.weight_block(wl.index, "w", N, K, b, "signs")
+        r0 = b * synth.ROW_BLOCK
+        B.bl_pack_w1(to_gpu(blk), out=wq[r0:r0 + blk.shape[0]])
+    ws = synth.block_scale_matrix(wl.index, N, K // G, tensor="group_scale")
+    xb = synth.activations(wl.index, M, K, "bf16")
+    q, s = O.quantize_act_absmax_int8(xb, "bf16")
+    y = B.bl_gemm_w1a8(to_gpu(q), to_gpu(s), wq, fp16_gpu(ws), group=G)
+    yb = bits16(y)
+    rows = np.unique(np.concatenate([[0, 1, N - 1, N - 2], rng(M).integers(0, N, 60)]))
+    wrows = synth.weight_rows(wl.index, "w", N, K, rows, "signs")
+    dref, yref, cond = O.gemm_w1a8(q, s, O.pack_w1(wrows), ws[rows], None, K, G)
+    assert_close(x_f64(yb[:, rows], "bf16"), yref, cond, TOL_BF16, "lm head M=%d" % M)
+
+
+# ---------------------------------------------------------------------------
+# i2_s x int8 (prefill)
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("M,N,K", [(1, 1, 128), (5, 70, 256), (128, 128, 1024), (130, 200, 2560), (512, 96, 384)])
+def test_gemm_i2s_int8_small(B, M, N, K):
+    g = rng(M + N + K)
+    w = ternary(g, N, K)
+    q, s = O.quantize_act_absmax_int8(rand_x(g, K, "bf16", M), "bf16")
+    sw = np.float32(g.uniform(0.5, 2))
+    packed = B.bl_pack_i2s(to_gpu(w), sw)
+    y, acc = B.bl_gemm_i2s_int8(to_gpu(q), to_gpu(s), packed, N, acc=True)
+    aref, yref, cond = O.gemm_i2s_int8(q, s, O.pack_i2s(w, sw), N, K)
+    assert np.array_equal(acc.cpu().numpy().astype(np.int64), aref), "accumulators must be bit-exact"
+    assert_close(y.cpu().numpy(), yref, cond, TOL_F32, "prefill %dx%dx%d" % (M, N, K))
+
+
+def test_gemm_i2s_int8_workload_prefill(B):
+    """M=512, 2560 -> 6912: all accumulators of sampled columns bit-exact; y within tolerance."""
+    wl = synth.WORKLOADS["i2s_prefill_512"]
+    M, N, K = wl.M, wl.N, wl.K
+    w = synth.weight_matrix(wl.index, "w", N, K, "ternary", wl.p_zero)
+    sw = synth.tensor_scale(wl.index)
+    q, s = O.quantize_act_absmax_int8(synth.activations(wl.index, M, K, "bf16"), "bf16")
+    packed = B.bl_pack_i2s(to_gpu(w), sw)
+    y, acc = B.bl_gemm_i2s_int8(to_gpu(q), to_gpu(s), packed, N, acc=True)
+    y2 = B.bl_gemm_i2s_int8(to_gpu(q), to_gpu(s), packed, N)
+    assert torch.equal(y, y2), "the y-only launch must match the launch that also writes acc"
+    rows = np.unique(np.concatenate([[0, N - 1], rng(9).integers(0, N, 62)]))
+    aref, yref, cond = O.gemm_i2s_int8(q, s, O.pack_i2s(w, sw), N, K, rows=rows)
+    assert np.array_equal(acc.cpu().numpy()[:, rows].astype(np.int64), aref)
+    assert_close(y.cpu().numpy()[:, rows], yref, cond, TOL_F32, "prefill workload")
+
+
+# ---------------------------------------------------------------------------
+# determinism, overlap switch, error paths
+# ---------------------------------------------------------------------------
+
+def test_repeated_calls_bitwise_identical(B):
+    g = rng(99)
+    N, K = 3000, 2560
+    w = ternary(g, N, K)
+    packed = B.bl_pack_i2s(to_gpu(w), 1.0)
+    x = x_gpu(rand_x(g, K, "bf16"), "bf16")
+    ys = [B.bl_gemv_i2s(packed, x, N, K) for _ in range(3)]
+    assert all(torch.equal(ys[0].view(torch.int16), t.view(torch.int16)) for t in ys[1:])
+    wb = synth.signs(g, (N, K))
+    wq = B.bl_pack_w1(to_gpu(wb))
+    q, s = O.quantize_act_absmax_int8(rand_x(g, K, "bf16", 4), "bf16")
+    ws = fp16_gpu(synth.abs_normal_fp16_bits(g, (N, K // 128), 0.02))
+    outs = [B.bl_gemm_w1a8(to_gpu(q), to_gpu(s), wq, ws) for _ in range(3)]
+    assert all(torch.equal(outs[0].view(torch.int16), t.view(torch.int16)) for t in outs[1:])
+
+
+def test_overlap_mode_same_results(B):
+    """With programmatic dependent launch enabled, back-to-back products give the same bits."""
+    g = rng(123)
+    N, K = 6912, 2560
+    w = ternary(g, N, K, 0.4)
+    packed = B.bl_pack_i2s(to_gpu(w), 0.75)
+    x = x_gpu(rand_x(g, K, "bf16"), "bf16")
+    torch.cuda.synchronize()
+    ref = B.bl_gemv_i2s(packed, x, N, K)
+    B.set_overlap(True)
+    try:
+        outs = [B.bl_gemv_i2s(packed, x, N, K) for _ in range(4)]
+    finally:
+        B.set_overlap(False)
+    torch.cuda.synchronize()
+    assert all(torch.equal(ref.view(torch.int16), t.view(torch.int16)) for t in outs)
+
+
+def test_error_paths(B):
+    x = torch.zeros(100, dtype=torch.float32, device="cuda")
+    p = torch.zeros(1000, dtype=torch.uint8, device="cuda")
+    with pytest.raises(B.BLError) as e:
+        B.bl_gemv_i2s(p, x, 4, 100)
+    assert e.value.status == B.BL_ERR_SHAPE
+    with pytest.raises(B.BLError) as e:
+        B.bl_gemv_i2s(p[1:], x, 4, 128)
+    assert e.value.status == B.BL_ERR_ALIGN
+    q = torch.zeros((9, 128), dtype=torch.int8, device="cuda")
+    with pytest.raises(B.BLError) as e:
+        B.bl_gemm_w1a8(q, torch.ones(9, device="cuda"), torch.zeros((4, 4), dtype=torch.int32, device="cuda"),
+                       torch.zeros((4, 1), dtype=torch.float16, device="cuda"))
+    assert e.value.status == B.BL_ERR_UNSUPPORTED
