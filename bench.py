@@ -1,0 +1,532 @@
+"""Benchmark of the packed BitLinear hot path on GB300.
+
+Headline workload (one step = the BitNet-2B-shaped MLP for one token):
+    gate  y_g = W_g x   (i2_s, 2560 -> 6912, bf16 in, bf16 out)
+    up    y_u = W_u x   (i2_s, 2560 -> 6912)
+    down  y_d = W_d x_d (i2_s, 6912 -> 2560, x_d a second bf16 vector)
+The three matrices are held in 24 rotating copies (320 MB, more than twice
+the 129 MB L2), so every step streams its weights from HBM.  Steps are
+captured in CUDA graphs (with programmatic dependent launch between the
+kernels) and replayed; the timed region is exactly --steps steps, bracketed by
+a barrier and a device synchronize, timed with CUDA events on the launching
+stream.
+
+metric: packed-weight GB/s = (packed i2_s bytes of the three matrices,
+scales included) * steps / time.  Secondary lines report the other
+workloads (i2_s fp32 2560x2560, TQ2_0 5120x13824, W1A8 LM head at M=1/4/8,
+i2_s int8 prefill at M=512 in TOPS).
+
+--impl reference times the CPU oracle (oracle/) on this machine's cores on
+a bounded sample of the same workload and prints the same JSON line.
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from gemm_bl_gemv_gb300 import synth  # noqa: E402
+
+METRIC = "M=1 packed-weight GB/s (% of HBM peak); M=512 int8 TOPS (% of peak)"
+UNIT = "GB/s"
+WL = synth.WORKLOADS["i2s_mlp_bitnet2b"]
+MATS = ("gate", "up", "down")
+COPIES = 24
+FALLBACK_HBM = 6800.0
+FALLBACK_BF16 = 1900.0
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), \
+            "measured"
+    return FALLBACK_HBM, FALLBACK_BF16, 1700.0, "fallback"
+
+
+def packed_bytes(N, K):
+    return N * (K // 4) + 4
+
+
+def mlp_bytes():
+    return sum(packed_bytes(*WL.extra[m]) for m in MATS)
+
+
+def mlp_algorithmic_bytes_per_launch():
+    """Per GEMV launch: packed weights + scale + x (bf16) + y (bf16), averaged over the three."""
+    tot = 0
+    for m in MATS:
+        N, K = WL.extra[m]
+        tot += packed_bytes(N, K) + 2 * K + 2 * N
+    return tot / 3.0
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (replicas: no collective on the data path)
+# ---------------------------------------------------------------------------
+
+class Dist:
+    def __init__(self, n_gpus):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+        if self.world > 1:
+            import torch.distributed as dist
+            dist.init_process_group("nccl")
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg:
+            import torch
+            self.pg.barrier()
+            torch.cuda.synchronize()
+
+    def max(self, v):
+        if not self.pg:
+            return v
+        import torch
+        t = torch.tensor([v], dtype=torch.float64, device="cuda")
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.pg:
+            self.pg.destroy_process_group()
+
+
+# ---------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# our implementation
+# ---------------------------------------------------------------------------
+
+def upload_i2s(B, torch, wl_index, tensor, N, K, p_zero, scale, copies):
+    """Pack one seeded ternary matrix on the GPU and replicate the packed bytes."""
+    w = synth.weight_matrix(wl_index, tensor, N, K, "ternary", p_zero)
+    packed = B.bl_pack_i2s(torch.from_numpy(w).cuda(), scale)
+    return [packed] + [packed.clone() for _ in range(copies - 1)]
+
+
+def time_graph(torch, dist, body, steps, warmup, graph_steps, stream):
+    """Capture `graph_steps` steps in a graph, replay: warm-up, then exactly `steps` timed steps."""
+    assert steps % graph_steps == 0 and warmup % graph_steps == 0
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        for i in range(2):  # eager warm-up (kernel attributes, lazy loading)
+            body(i)
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(graph_steps):
+                body(i)
+    with torch.cuda.stream(stream):  # replay() launches on the current stream
+        for _ in range(warmup // graph_steps):
+            g.replay()
+        torch.cuda.synchronize()
+        dist.barrier()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps // graph_steps):
+            g.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    dist.barrier()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1)
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "gemm_bl_gemv_gb300", "csrc")
+    for f in ("gemv_i2s.cu", "gemv_tiled.cuh", "bl_device.cuh"):
+        h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic():
+    """dram bytes per launch of the dominant kernel from the committed ncu summary, or None
+    when the kernel source changed since the counters were taken."""
+    p = os.path.join(ROOT, "profiles", "gemv_i2s_mlp_bitnet2b.md")
+    if not os.path.exists(p):
+        return None
+    vals = {}
+    for line in open(p):
+        if ":" in line and line.strip().startswith("- "):
+            k, v = line.strip()[2:].split(":", 1)
+            vals[k.strip()] = v.strip().strip("`")
+    if vals.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    try:
+        return float(vals["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+def bench_ours(args, dist):
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    from gemm_bl_gemv_gb300 import binding as B
+
+    torch.cuda.set_device(dist.local)
+    hbm, bf16_burst, bf16_sust, peak_src = peaks()
+    stream = torch.cuda.Stream()
+    B.set_overlap(True)
+
+    # ---- headline: BitNet-2B MLP, M=1, bf16 -----------------------------------------
+    with torch.cuda.stream(stream):
+        mats = {}
+        for m in MATS:
+            N, K = WL.extra[m]
+            mats[m] = upload_i2s(B, torch, WL.index, "w_" + m, N, K, WL.p_zero,
+                                 synth.tensor_scale(WL.index, "scale_" + m), COPIES)
+        x_bits = synth.activations(WL.index, 1, 2560, "bf16")[0]
+        xd_bits = synth.activations(WL.index, 1, 6912, "bf16", tensor="x_down")[0]
+        x = torch.from_numpy(x_bits.view(np.int16)).cuda().view(torch.bfloat16)
+        xd = torch.from_numpy(xd_bits.view(np.int16)).cuda().view(torch.bfloat16)
+        yg = torch.empty(6912, dtype=torch.bfloat16, device="cuda")
+        yu = torch.empty(6912, dtype=torch.bfloat16, device="cuda")
+        ydn = torch.empty(2560, dtype=torch.bfloat16, device="cuda")
+    torch.cuda.synchronize()
+
+    def mlp_step(i):
+        c = i % COPIES
+        B.bl_gemv_i2s(mats["gate"][c], x, 6912, 2560, y=yg)
+        B.bl_gemv_i2s(mats["up"][c], x, 6912, 2560, y=yu)
+        B.bl_gemv_i2s(mats["down"][c], xd, 2560, 6912, y=ydn)
+
+    gs = args.graph_steps
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        ms = time_graph(torch, dist, mlp_step, args.steps, args.warmup, gs, stream)
+    ms = dist.max(ms)
+    step_bytes = mlp_bytes()
+    value = step_bytes * args.steps * dist.world / (ms * 1e-3) / 1e9
+    launches = 3 * args.steps
+    avg_launch_s = ms * 1e-3 / launches
+    achieved = mlp_algorithmic_bytes_per_launch() / avg_launch_s / 1e9
+
+    # ---- e2e: host buffers, copies inside the timed region, public API per step -------
+    e2e_steps = min(args.steps, args.e2e_steps)
+    hx = torch.from_numpy(x_bits.view(np.int16).copy()).pin_memory()
+    hxd = torch.from_numpy(xd_bits.view(np.int16).copy()).pin_memory()
+    hyg = torch.empty(6912, dtype=torch.int16).pin_memory()
+    hyu = torch.empty(6912, dtype=torch.int16).pin_memory()
+    hyd = torch.empty(2560, dtype=torch.int16).pin_memory()
+    dx = torch.empty(2560, dtype=torch.int16, device="cuda")
+    dxd = torch.empty(6912, dtype=torch.int16, device="cuda")
+
+    def e2e_step(i):
+        c = i % COPIES
+        dx.copy_(hx, non_blocking=True)
+        dxd.copy_(hxd, non_blocking=True)
+        B.bl_gemv_i2s(mats["gate"][c], dx.view(torch.bfloat16), 6912, 2560, y=yg)
+        B.bl_gemv_i2s(mats["up"][c], dx.view(torch.bfloat16), 6912, 2560, y=yu)
+        B.bl_gemv_i2s(mats["down"][c], dxd.view(torch.bfloat16), 2560, 6912, y=ydn)
+        hyg.copy_(yg.view(torch.int16), non_blocking=True)
+        hyu.copy_(yu.view(torch.int16), non_blocking=True)
+        hyd.copy_(ydn.view(torch.int16), non_blocking=True)
+
+    B.set_overlap(False)
+    with torch.cuda.stream(stream):
+        for i in range(min(200, e2e_steps)):
+            e2e_step(i)
+        torch.cuda.synchronize()
+        dist.barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(e2e_steps):
+            e2e_step(i)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        dist.barrier()
+    e2e_ms = dist.max(e0.elapsed_time(e1))
+    e2e_value = step_bytes * e2e_steps * dist.world / (e2e_ms * 1e-3) / 1e9
+    h2d = 2 * (2560 + 6912)
+    d2h = 2 * (6912 + 6912 + 2560)
+    B.set_overlap(True)
+
+    extra = {}
+    if not args.no_extra:
+        extra = bench_secondary(args, B, torch, stream, dist, hbm, bf16_burst)
+    del mats
+    torch.cuda.empty_cache()
+
+    cpu = None
+    if dist.rank == 0 and dist.world == 1 and args.cpu_seconds > 0:
+        cpu = cpu_baseline(args.cpu_seconds)
+
+    if dist.rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": dist.world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "int8xint8->int32 (dp4a), fp32 epilogue", "data": "synthetic",
+            "config": {"workload": WL.name, "model": "BitNet-2B-shaped MLP (random ternary weights)",
+                       "global_batch": 1, "seq_len": 1, "parallelism": "replicas" if dist.world > 1 else "single",
+                       "M": 1, "shapes_NxK": [list(WL.extra[m]) for m in MATS], "x": "bf16", "y": "bf16",
+                       "weight_copies": COPIES, "l2": "inputs larger than L2 (24 rotating weight copies, 320 MB)",
+                       "launch": "CUDA graph of %d steps, programmatic dependent launch" % gs},
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+                         "frac": round(achieved / hbm, 4), "traffic": profiled_traffic(),
+                         "kernel": "tiled_kernel<I2sPolicy<3,bf16,bf16>>",
+                         "algorithmic_bytes_per_launch": mlp_algorithmic_bytes_per_launch(),
+                         "peak_source": peak_src + " copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"},
+            "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "steps": e2e_steps, "api": "gemm_bl_gemv_gb300.binding.bl_gemv_i2s per call, eager"},
+            "gpu_launches": launches,
+            "clocks": clk.summary(),
+            "cpu_baseline": cpu,
+            "secondary": extra,
+        }
+        print(json.dumps(line))
+
+
+def bench_secondary(args, B, torch, stream, dist, hbm, bf16_peak):
+    """Other workloads: single-workload GB/s (or TOPS) with rotating copies, graphs + PDL."""
+    out = {}
+    gs = 100
+    steps = max(gs, (args.secondary_steps // gs) * gs)
+
+    def run(body):
+        return dist.max(time_graph(torch, dist, body, steps, gs, gs, stream)) / steps  # ms per step
+
+    with torch.cuda.stream(stream):
+        # i2_s GEMV 2560x2560 fp32
+        wl = synth.WORKLOADS["i2s_gemv_2560"]
+        cps = 160
+        ws = upload_i2s(B, torch, wl.index, "w", wl.N, wl.K, wl.p_zero, synth.tensor_scale(wl.index), cps)
+        x = torch.from_numpy(synth.activations(wl.index, 1, wl.K, "f32")[0]).cuda()
+        y = torch.empty(wl.N, dtype=torch.float32, device="cuda")
+        t = run(lambda i: B.bl_gemv_i2s(ws[i % cps], x, wl.N, wl.K, y=y))
+        gbs = packed_bytes(wl.N, wl.K) / (t * 1e-3) / 1e9
+        out[wl.name] = {"value": round(gbs, 1), "unit": "GB/s", "frac_hbm": round(gbs / hbm, 4), "us_per_launch": t * 1e3}
+        del ws
+
+        # TQ2_0 GEMV 5120 -> 13824, bf16 x, fp32 y
+        wl = synth.WORKLOADS["tq2_0_gemv_5120x13824"]
+        cps = 16
+        w = synth.weight_matrix(wl.index, "w", wl.N, wl.K, "ternary", wl.p_zero)
+        d = synth.block_scale_matrix(wl.index, wl.N, wl.K // 256)
+        p0 = B.bl_pack_tq2_0(torch.from_numpy(w).cuda(), torch.from_numpy(d.view(np.int16)).cuda())
+        ws = [p0] + [p0.clone() for _ in range(cps - 1)]
+        x = torch.from_numpy(synth.activations(wl.index, 1, wl.K, "bf16")[0].view(np.int16)).cuda().view(torch.bfloat16)
+        y = torch.empty(wl.N, dtype=torch.float32, device="cuda")
+        t = run(lambda i: B.bl_gemv_tq2_0(ws[i % cps], x, wl.N, wl.K, y=y))
+        nbytes = wl.N * (wl.K // 256) * 66
+        gbs = nbytes / (t * 1e-3) / 1e9
+        out[wl.name] = {"value": round(gbs, 1), "unit": "GB/s", "frac_hbm": round(gbs / hbm, 4), "us_per_launch": t * 1e3}
+        del ws, p0
+
+        # W1A8 LM head, M = 1, 4, 8
+        wl = synth.WORKLOADS["w1a8_lmhead_248320"]
+        N, K, G = wl.N, wl.K, wl.group
+        wq = torch.empty((N, K // 32), dtype=torch.int32, device="cuda")
+        for b in range((N + synth.ROW_BLOCK - 1) // synth.ROW_BLOCK):
+            blk = synth.weight_block(wl.index, "w", N, K, b, "signs")
+            B.bl_pack_w1(torch.from_numpy(blk).cuda(), out=wq[b * synth.ROW_BLOCK:b * synth.ROW_BLOCK + blk.shape[0]])
+        wsc = torch.from_numpy(synth.block_scale_matrix(wl.index, N, K // G, tensor="group_scale").view(np.int16)).cuda()
+        wqs, wss = [wq, wq.clone()], [wsc, wsc.clone()]
+        wbytes = N * K // 8 + N * (K // G) * 2
+        for M in (1, 4, 8):
+            xb = synth.activations(wl.index, M, K, "bf16")
+            q, s = B.bl_quantize_act_absmax_int8(torch.from_numpy(xb.view(np.int16)).cuda().view(torch.bfloat16))
+            y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+            t = run(lambda i: B.bl_gemm_w1a8(q, s, wqs[i % 2], wss[i % 2].view(torch.float16), group=G, y=y))
+            gbs = wbytes / (t * 1e-3) / 1e9
+            out["%s_M%d" % (wl.name, M)] = {"value": round(gbs, 1), "unit": "GB/s", "frac_hbm": round(gbs / hbm, 4),
+                                            "us_per_launch": t * 1e3,
+                                            "int_ops_per_s": 2.0 * M * N * K / (t * 1e-3)}
+        del wqs, wss, wq, wsc
+
+        # i2_s int8 prefill M = 512 (tensor-bound: TOPS)
+        wl = synth.WORKLOADS["i2s_prefill_512"]
+        cps = 24
+        ws = upload_i2s(B, torch, wl.index, "w", wl.N, wl.K, wl.p_zero, synth.tensor_scale(wl.index), cps)
+        xb = synth.activations(wl.index, wl.M, wl.K, "bf16")
+        q, s = B.bl_quantize_act_absmax_int8(torch.from_numpy(xb.view(np.int16)).cuda().view(torch.bfloat16))
+        y = torch.empty((wl.M, wl.N), dtype=torch.float32, device="cuda")
+        t = run(lambda i: B.bl_gemm_i2s_int8(q, s, ws[i % cps], wl.N, y=y))
+        tops = 2.0 * wl.M * wl.N * wl.K / (t * 1e-3) / 1e12
+        out[wl.name] = {"value": round(tops, 2), "unit": "TOPS (int8 ops)", "frac_bf16_dense_peak": round(tops / bf16_peak, 4),
+                        "us_per_launch": t * 1e3}
+        del ws
+    torch.cuda.synchronize()
+    return out
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle (baseline leg and reference arm)
+# ---------------------------------------------------------------------------
+
+class OracleMLP:
+    """The oracle computing the MLP step on `rows_frac` of each matrix's rows."""
+
+    def __init__(self, rows_frac=1.0):
+        from oracle import oracle as O
+        self.O = O
+        self.cores = len(os.sched_getaffinity(0))
+        O.set_threads(self.cores)
+        self.mats = {}
+        for m in MATS:
+            N, K = WL.extra[m]
+            w = synth.weight_matrix(WL.index, "w_" + m, N, K, "ternary", WL.p_zero)
+            nr = max(1, int(round(N * rows_frac)))
+            rows = np.linspace(0, N - 1, nr).astype(np.int64)
+            self.mats[m] = (O.pack_i2s(w, synth.tensor_scale(WL.index, "scale_" + m)), N, K, rows)
+        xb = synth.activations(WL.index, 1, 2560, "bf16")[0]
+        xdb = synth.activations(WL.index, 1, 6912, "bf16", tensor="x_down")[0]
+        self.x = O.bf16_to_f64(xb)
+        self.xd = O.bf16_to_f64(xdb)
+        self.bytes_per_step = sum(len(r) * (K // 4) for (_, _, K, r) in self.mats.values())
+
+    def step(self):
+        for m in MATS:
+            p, N, K, rows = self.mats[m]
+            self.O.gemv_i2s(p, self.x if m != "down" else self.xd, N, K, rows=rows)
+
+
+def cpu_baseline(seconds):
+    o = OracleMLP(1.0)
+    o.step()
+    t0 = time.perf_counter()
+    n = 0
+    while time.perf_counter() - t0 < seconds:
+        o.step()
+        n += 1
+    dt = time.perf_counter() - t0
+    return {"value": round(o.bytes_per_step * n / dt / 1e9, 4), "unit": UNIT, "cores": o.cores if o.O.has_openmp() else 1,
+            "kind": "oracle",
+            "sample": "%d full MLP steps (gate+up+down, all rows, one token) in %.1f s" % (n, dt)}
+
+
+def bench_reference(args, dist):
+    if dist.rank != 0:
+        return
+    probe = OracleMLP(1.0)
+    probe.step()
+    t0 = time.perf_counter()
+    probe.step()
+    t_full = time.perf_counter() - t0
+    budget = args.ref_seconds / max(1, args.steps + args.warmup)
+    frac = min(1.0, max(1e-4, budget / max(t_full, 1e-9)))
+    o = OracleMLP(frac)
+    for _ in range(args.warmup):
+        o.step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        o.step()
+    dt = time.perf_counter() - t0
+    value = o.bytes_per_step * args.steps / dt / 1e9
+    cores = o.cores if o.O.has_openmp() else 1
+    line = {
+        "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": dist.world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64 (oracle)", "data": "synthetic", "impl": "reference",
+        "config": {"workload": WL.name, "model": "BitNet-2B-shaped MLP (random ternary weights)", "global_batch": 1,
+                   "seq_len": 1, "parallelism": "single", "M": 1},
+        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": "each step: the MLP on %.4f of each matrix's rows" % frac},
+        "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200000)
+    ap.add_argument("--warmup", type=int, default=4000)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--graph-steps", type=int, default=1000)
+    ap.add_argument("--e2e-steps", type=int, default=20000)
+    ap.add_argument("--secondary-steps", type=int, default=2000)
+    ap.add_argument("--no-extra", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--ref-seconds", type=float, default=60.0)
+    args = ap.parse_args()
+    dist = Dist(args.gpus)
+    try:
+        if args.impl == "reference":
+            bench_reference(args, dist)
+        else:
+            gs = min(args.graph_steps, args.steps)
+            while args.steps % gs or args.warmup % gs:
+                gs -= 1
+            args.graph_steps = gs
+            if args.warmup < 3:
+                args.warmup = 3 * gs if 3 * gs >= 3 else 3
+            bench_ours(args, dist)
+    finally:
+        dist.close()
+
+
+if __name__ == "__main__":
+    main()

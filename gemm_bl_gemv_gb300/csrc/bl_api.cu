@@ -54,6 +54,22 @@ unsigned int* dev_error_ptr() {
   return cache[dev];
 }
 
+cudaError_t raise_smem_cap_impl(const void* kernel, int dev, int bytes) {
+  struct Entry {
+    const void* k;
+    int dev, bytes;
+  };
+  static Entry entries[256];
+  static int n = 0;
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lock(mu);
+  for (int i = 0; i < n; ++i)
+    if (entries[i].k == kernel && entries[i].dev == dev && entries[i].bytes >= bytes) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && n < 256) entries[n++] = Entry{kernel, dev, bytes};
+  return e;
+}
+
 int sm_count() {
   static int cache[64] = {0};
   int dev = 0;
@@ -149,7 +165,7 @@ bl_status bl_gemv_i2s(const uint8_t* packed, const void* x, bl_dtype xt, void* y
     return fail(BL_ERR_DTYPE, "bl_gemv_i2s: bad dtype (x %d, y %d)", int(xt), int(yt));
   if (N < 1 || K < 128 || K % 128 || N > 0x7fffffff)
     return fail(BL_ERR_SHAPE, "bl_gemv_i2s: need N >= 1, K %% 128 == 0 (N=%lld K=%lld)", (long long)N, (long long)K);
-  if (K / 128 > 1024) return fail(BL_ERR_UNSUPPORTED, "bl_gemv_i2s: K up to 131072 supported (K=%lld)", (long long)K);
+  if (K > 32768) return fail(BL_ERR_UNSUPPORTED, "bl_gemv_i2s: K up to 32768 supported (K=%lld)", (long long)K);
   if (!aligned(packed, 16)) return fail(BL_ERR_ALIGN, "bl_gemv_i2s: packed must be 16-byte aligned");
   if (!aligned(x, xt == BL_F32 ? 4 : 2) || !aligned(y, yt == BL_F32 ? 4 : 2))
     return fail(BL_ERR_ALIGN, "bl_gemv_i2s: x and y must be aligned to their element size");

@@ -98,6 +98,23 @@ __device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
   return d;
 }
 
+// sum over 4 bytes of (unsigned a_i) * (unsigned b_i) + c
+__device__ __forceinline__ int dp4a_uu(uint32_t a, uint32_t b, int c) {
+  int d;
+  asm("dp4a.u32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
+// 2^n as fp32 for n in [-126, 127] (built from the exponent field)
+__device__ __forceinline__ float exp2i(int n) { return __int_as_float((127 + n) << 23); }
+
+// Exponent e with 0 < m < 2^e and m >= 2^(e-1), for a positive finite float m.
+__device__ __forceinline__ int exponent_of(float m) {
+  const uint32_t b = __float_as_uint(m);
+  const int E = int(b >> 23);
+  return E ? E - 126 : (32 - __clz(int(b & 0x7FFFFFu))) - 149;
+}
+
 __device__ __forceinline__ float bf16_bits_to_f32(uint16_t b) { return __uint_as_float(uint32_t(b) << 16); }
 
 __device__ __forceinline__ uint16_t f32_to_bf16_bits_rn(float f) {
@@ -110,6 +127,29 @@ __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
   return v;
+}
+
+// One-instruction warp reductions (redux.sync).
+__device__ __forceinline__ int redux_add(int v) {
+  int r;
+  asm volatile("redux.sync.add.s32 %0, %1, 0xffffffff;" : "=r"(r) : "r"(v));
+  return r;
+}
+__device__ __forceinline__ uint32_t redux_max_u32(uint32_t v) {
+  uint32_t r;
+  asm volatile("redux.sync.max.u32 %0, %1, 0xffffffff;" : "=r"(r) : "r"(v));
+  return r;
+}
+
+__device__ __forceinline__ int warp_sum_int(int v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// Barrier over `nthreads` threads (a multiple of 32) of the CTA, id 1..15.
+__device__ __forceinline__ void named_barrier_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
 __device__ __forceinline__ float warp_max(float v) {

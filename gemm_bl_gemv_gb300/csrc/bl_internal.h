@@ -1,6 +1,7 @@
 // Host-side internals of libbl: launch functions called by the C ABI layer.
 #pragma once
 #include <cstdint>
+#include <mutex>
 #include <utility>
 #include <cuda_runtime.h>
 
@@ -18,6 +19,47 @@ int sm_count();
 // BL_DEVERR_* bits read by bl_device_error()); kernels receive it as an
 // argument.  nullptr if it cannot be resolved.
 unsigned int* dev_error_ptr();
+
+// Launch plans (geometry, grid, kernel attributes already set) remembered per
+// (device, N, K) so that repeated calls skip the occupancy queries.
+template <class P>
+class PlanCache {
+ public:
+  bool get(int dev, int64_t N, int64_t K, P* out) {
+    std::lock_guard<std::mutex> lock(mu_);
+    for (int i = 0; i < n_; ++i)
+      if (e_[i].dev == dev && e_[i].N == N && e_[i].K == K) {
+        *out = e_[i].p;
+        return true;
+      }
+    return false;
+  }
+  void put(int dev, int64_t N, int64_t K, const P& p) {
+    std::lock_guard<std::mutex> lock(mu_);
+    const int i = n_ < kSize ? n_++ : (next_++ % kSize);
+    e_[i] = Entry{dev, N, K, p};
+  }
+
+ private:
+  static constexpr int kSize = 64;
+  struct Entry {
+    int dev;
+    int64_t N, K;
+    P p;
+  };
+  Entry e_[kSize];
+  int n_ = 0, next_ = 0;
+  std::mutex mu_;
+};
+
+// Set a kernel's dynamic shared memory cap to `bytes` on device `dev` once.
+// The cap belongs to the kernel function (not to a launch), so it is set to
+// the largest size any plan may use rather than to one plan's size.
+cudaError_t raise_smem_cap_impl(const void* kernel, int dev, int bytes);
+template <typename... KArgs>
+cudaError_t raise_smem_cap(void (*kernel)(KArgs...), int dev, int bytes) {
+  return raise_smem_cap_impl(reinterpret_cast<const void*>(kernel), dev, bytes);
+}
 
 // Launch helper: cudaLaunchKernelEx with the PDL attribute when overlap is on.
 template <typename... KArgs, typename... Args>

@@ -2,228 +2,365 @@
 // ("Hesper/Layers/BitLinear", sections "i2_s Packing Format" and
 // "BitLinear Mathematics").
 //
-// Decode.  A 32-bit word of a 128-element group holds bytes p..p+3 of the
-// group; bits (7-2t):(6-2t) of byte p are the code of element 32t+p.  For
-// the four shift classes we form byte masks of the codes:
-//   class 0 (shift 0, elements 96+p): w & 0x03030303          -> code
-//   class 1 (shift 2, elements 64+p): (w >> 2) & 0x03030303   -> code
-//   class 2 (shift 4, elements 32+p): w & 0x30303030          -> 16*code
-//   class 3 (shift 6, elements p)   : (w >> 2) & 0x30303030   -> 16*code
-// and feed them to dp4a against activation digits.  Codes are c = w + 1, so
-//   sum_k w_k X_k = sum_k c_k X_k - sum_k X_k,
-// the second sum being the same for every row.
+// Work decomposition.  A warp owns a tile of 16 rows: lanes l and l+16 both
+// work on row l of the tile and take alternate 128-element groups of the
+// warp's group range; their sums are added with one shuffle.  When rows are
+// few the group range of a tile is split over `wk` warps of the CTA and
+// their row sums are added in warp order.  Each row's slice is bulk-copied
+// (cp.async.bulk) into a shared-memory row whose stride is an odd number of
+// 16-byte units, so the 128-bit reads of every 8-lane phase hit distinct
+// banks.  The activation digits of a group are read by broadcast (at most
+// two addresses per instruction).  Row tiles of a warp stream through a ring
+// of `stages` buffers completed by mbarriers (bounded waits).  The
+// activation vector itself arrives by one bulk copy issued right after the
+// wait on the previous kernel.
 //
-// Activations.  x is turned, once per CTA, into exact fixed-point integers
-// X = rint(x * 2^F_c) with one exponent F_c per 128-element group c, chosen
-// from the group's max|x| so that |X| < 2^(8D-2), and stored as D balanced
-// int8 digits (X = sum_d digit_d 256^d).  D = 4 for fp32 input (30-bit
-// magnitude: fp32 values within 6 binades of the group maximum are carried
-// exactly, smaller ones with absolute error <= 2^-31 * group max), D = 3
-// for bf16 input (exact within 14 binades).  Products and sums over a group
-// are exact integers; the group sum is converted to fp32 once.
+// Decode.  A 32-bit word of a group holds bytes p..p+3; bits (7-2t):(6-2t)
+// of byte p are the code of element 32t+p.  Byte masks of the codes:
+//   shift 0 (elements 96+p): w & 0x03030303         -> code
+//   shift 2 (elements 64+p): (w >> 2) & 0x03030303  -> code
+//   shift 4 (elements 32+p): w & 0x30303030         -> 16*code
+//   shift 6 (elements p)   : (w >> 2) & 0x30303030  -> 16*code
+// go to dp4a against the activation digits of those elements.  Codes are
+// c = w + 1, so sum_k w_k X_k = sum_k c_k X_k - sum_k X_k.
+//
+// Activations.  Once per CTA, x is turned into exact fixed-point integers
+// X = rint(x * 2^F_g) with one exponent per 128-element group g chosen from
+// the group's max|x| so that |X| < 2^(8D-1), and stored as the D bytes of X
+// in two's complement (X = sum_{d<D-1} u_d 256^d + s_{D-1} 256^(D-1) with
+// unsigned low bytes u_d and a signed top byte).  D = 4 for fp32 input
+// (fp32 values within 7 binades of the group maximum are carried exactly,
+// smaller ones with absolute error <= 2^-32 * 2^ceil(log2 max)), D = 3 for
+// bf16 input (exact within 15 binades).  Products and sums over a group are
+// exact integers; each group sum is converted to fp32 once, scaled by
+// 2^-F_g and added.
+#include <algorithm>
+
+#include "bl_device.cuh"
 #include "bl_internal.h"
-#include "gemv_tiled.cuh"
 
 namespace bl {
 namespace {
 
-constexpr int kI2sR = 4;
+constexpr int kRows = 16;  // rows per warp tile (two lanes per row)
+
+struct Geom {
+  int N, K, nC;        // rows, columns, 128-element groups per row
+  int wk, wr;          // warps per row tile (K split), row tiles per CTA
+  int stages;          // ring depth per warp
+  int ntiles;          // ceil(N / kRows)
+  int rowstride;       // bytes per row in a ring buffer (odd multiple of 16)
+  int xbytes;          // bytes of x (K * element size)
+  uint32_t stage_bytes;
+  uint32_t off_bar, off_stage, off_part, off_x, off_xraw, smem;
+  unsigned int* err;
+};
+
+// Per-group activation record: [8 words][4 shifts][D digits] u32, then D
+// digit sums (int) and two fp32 factors whose product is 2^-F_g.
+template <int D>
+struct Rec {
+  static constexpr int kWords = (32 * D + D + 2 + 3) / 4 * 4;  // u32 per record, 16-byte multiple
+};
+
+template <int D, bool XB>
+__device__ __forceinline__ void prepare_x(const void* xv, int nC, uint32_t* xrec, int warp, int nwarps, int lane) {
+  constexpr int RW = Rec<D>::kWords;
+  for (int c = warp; c < nC; c += nwarps) {
+    // lane l holds elements 4l..4l+3 of group c: shift class t = l/8
+    // (elements 32t..32t+31), bytes 4w..4w+3 with w = l%8.  xv is 8-byte
+    // (bf16) or 16-byte (fp32) aligned here.
+    float v[4];
+    const int e0 = c * 128 + 4 * lane;
+    if (XB) {
+      const uint2 u = *reinterpret_cast<const uint2*>(reinterpret_cast<const uint16_t*>(xv) + e0);
+      v[0] = __uint_as_float(u.x << 16);
+      v[1] = __uint_as_float(u.x & 0xFFFF0000u);
+      v[2] = __uint_as_float(u.y << 16);
+      v[3] = __uint_as_float(u.y & 0xFFFF0000u);
+    } else {
+      const float4 u = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(xv) + e0);
+      v[0] = u.x; v[1] = u.y; v[2] = u.z; v[3] = u.w;
+    }
+    // non-negative floats order like their bit patterns
+    const float m = __uint_as_float(redux_max_u32(
+        __float_as_uint(fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3]))))));
+    const int F = m > 0.f ? (8 * D - 1) - exponent_of(m) : 0;
+    // x * 2^F as two exact power-of-two multiplies (each factor a normal float)
+    const int fa = F / 2, fb = F - fa;
+    const float sA = exp2i(fa), sB = exp2i(fb);
+    int X[4];
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      constexpr int kLim = int((1u << (8 * D - 1)) - 1u);  // keep the top byte signed
+      X[b] = max(-kLim, min(kLim, __float2int_rn(__fmul_rn(__fmul_rn(v[b], sA), sB))));
+    }
+    uint32_t* rec = xrec + c * RW;
+    const int t = lane >> 3, w = lane & 7, sh = 3 - t;
+#pragma unroll
+    for (int d = 0; d < D; ++d) {
+      // byte d of the four values, element b in byte b
+      const uint32_t sel = uint32_t(d) | (uint32_t(d + 4) << 4);
+      const uint32_t lo = __byte_perm(uint32_t(X[0]), uint32_t(X[1]), sel);
+      const uint32_t hi = __byte_perm(uint32_t(X[2]), uint32_t(X[3]), sel);
+      const uint32_t dig = __byte_perm(lo, hi, 0x5410);
+      rec[(w * 4 + sh) * D + d] = dig;
+      const int s = redux_add(d == D - 1 ? dp4a_us(0x01010101u, dig, 0) : dp4a_uu(0x01010101u, dig, 0));
+      if (lane == 0) reinterpret_cast<int*>(rec)[32 * D + d] = s;
+    }
+    if (lane == 0) {
+      reinterpret_cast<float*>(rec)[32 * D + D] = exp2i(-fa);
+      reinterpret_cast<float*>(rec)[32 * D + D + 1] = exp2i(-fb);
+    }
+  }
+}
 
 template <int D, bool XB, bool YB>
-struct I2sPolicy {
-  static constexpr int kMaxThreads = 1024;
-  struct Args {
-    const uint8_t* packed;
-    const void* x;
-    void* y;
-    int N, K;
+__global__ void __launch_bounds__(512) gemv_i2s_kernel(const uint8_t* __restrict__ packed, const void* __restrict__ x,
+                                                       void* __restrict__ y, Geom g, int early_weights) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  constexpr int RW = Rec<D>::kWords;
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const int nwarps = blockDim.x >> 5;
+  const int rt = warp / g.wk;  // row tile slot of this warp
+  const int ks = warp % g.wk;  // group range of this warp
+  const int c0 = ks * g.nC / g.wk, c1 = (ks + 1) * g.nC / g.wk;
+  const int nchunks = c1 - c0;
+  const int r = lane & (kRows - 1);  // row of the tile
+  const int u = lane >> 4;            // which alternate groups
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + g.off_bar) + warp * g.stages;
+  uint64_t* xbar = reinterpret_cast<uint64_t*>(smem + g.off_bar) + nwarps * g.stages;
+  uint64_t* tbar = xbar + 1 + rt;  // row-tile slot barrier: the wk warps of a tile meet here
+  uint8_t* ring = smem + g.off_stage + size_t(warp) * g.stages * g.stage_bytes;
+  float* part = reinterpret_cast<float*>(smem + g.off_part);
+  uint32_t* xrec = reinterpret_cast<uint32_t*>(smem + g.off_x);
+  uint8_t* xraw = smem + g.off_xraw;
+  __shared__ int abort_flag;
+
+  const int tile_stride = int(gridDim.x) * g.wr;
+  const int first = int(blockIdx.x) * g.wr + rt;
+  const int my_tiles = first < g.ntiles ? (g.ntiles - 1 - first) / tile_stride + 1 : 0;
+  const uint32_t slice_bytes = uint32_t(nchunks) * 32;
+  const int64_t row_bytes = g.K / 4;
+
+  // lanes 0..15 copy their row's group range of local tile i into ring buffer i % stages
+  auto issue = [&](int i) {
+    const int t = first + i * tile_stride;
+    const int s = i % g.stages;
+    const int row = t * kRows + r;
+    const int nrows = min(kRows, g.N - t * kRows);
+    if (lane == 0) mbar_arrive_expect_tx(&full[s], uint32_t(nrows) * slice_bytes);
+    __syncwarp();
+    if (u == 0 && row < g.N)
+      bulk_g2s(ring + size_t(s) * g.stage_bytes + size_t(r) * g.rowstride, packed + int64_t(row) * row_bytes + 32 * c0,
+               slice_bytes, &full[s], policy_evict_first());
   };
-  // policy area: [xd: 8 steps x 4 classes x D x nC u32][sumx: D x nC][fexp: nC][cmax: nC][consts: 8]
-  static __host__ __device__ uint32_t xd_words(int nC) { return 8u * 4u * D * nC; }
-  static __host__ __device__ uint32_t bytes(int nC) { return (xd_words(nC) + D * nC + 2 * nC + 8) * 4; }
 
-  static __device__ const uint8_t* weights(const Args& a) { return a.packed; }
-  static __device__ const uint8_t* aux(const Args&) { return nullptr; }
-
-  static __device__ float load_x(const Args& a, int e) {
-    if (XB) return bf16_bits_to_f32(reinterpret_cast<const uint16_t*>(a.x)[e]);
-    return reinterpret_cast<const float*>(a.x)[e];
+  if (lane == 0)
+    for (int s = 0; s < g.stages; ++s) mbar_init(&full[s], 1);
+  if (threadIdx.x == 0) {
+    mbar_init(xbar, 1);
+    for (int k = 0; k < g.wr; ++k) mbar_init(xbar + 1 + k, 32 * g.wk);
+    abort_flag = 0;
   }
+  fence_barrier_init();
+  __syncthreads();
+  const int npre = min(my_tiles, g.stages);
+  if (early_weights)
+    for (int i = 0; i < npre; ++i) issue(i);
+  pdl_wait();
+  // activations: one bulk copy when aligned, else plain loads into the same buffer
+  const bool x_bulk = (reinterpret_cast<uintptr_t>(x) & 15) == 0;
+  if (threadIdx.x == 0 && x_bulk) {
+    mbar_arrive_expect_tx(xbar, uint32_t(g.xbytes));
+    bulk_g2s(xraw, x, uint32_t(g.xbytes), xbar, policy_evict_first());
+  }
+  if (!early_weights)
+    for (int i = 0; i < npre; ++i) issue(i);
+  if (x_bulk) {
+    if (!mbar_wait_bounded(xbar, 0, g.err)) abort_flag = 1;
+  } else {
+    for (int k = threadIdx.x; k < g.xbytes / 2; k += blockDim.x)
+      reinterpret_cast<uint16_t*>(xraw)[k] = reinterpret_cast<const uint16_t*>(x)[k];
+    __syncthreads();
+  }
+  prepare_x<D, XB>(xraw, g.nC, xrec, warp, nwarps, lane);
+  const float wscale = *reinterpret_cast<const float*>(packed + int64_t(g.N) * row_bytes);
+  __syncthreads();
+  pdl_launch_dependents();
 
-  static __device__ void prepare(const Args& a, const TileGeom& g, uint8_t* smem, int tid, int T) {
-    const int nC = g.nC;
-    uint32_t* xd = reinterpret_cast<uint32_t*>(smem + g.off_pol);
-    int* sumx = reinterpret_cast<int*>(xd + xd_words(nC));
-    int* fexp = sumx + D * nC;
-    int* cmax = fexp + nC;
-    float* consts = reinterpret_cast<float*>(cmax + nC);
-    for (int c = tid; c < nC; c += T) cmax[c] = 0;
-    if (tid == 0) consts[1] = *reinterpret_cast<const float*>(a.packed + int64_t(a.N) * (a.K / 4));
-    __syncthreads();
-    // pass 1: max |x| of every 128-element group (non-negative floats order as ints)
-    for (int qd = tid; qd < a.K / 4; qd += T) {
-      float m = 0.f;
+  for (int i = 0; i < my_tiles; ++i) {
+    const int s = i % g.stages;
+    const int t = first + i * tile_stride;
+    if (!abort_flag && !mbar_wait_bounded(&full[s], uint32_t(i / g.stages) & 1u, g.err)) abort_flag = 1;
+    __syncwarp();
+    const uint8_t* myrow = ring + size_t(s) * g.stage_bytes + size_t(r) * g.rowstride;
+    float yacc = 0.f;
+    for (int cc = u; cc < nchunks; cc += 2) {
+      const uint32_t* rec = xrec + (c0 + cc) * RW;
+      // two independent accumulator sets (one per 16-byte half) shorten the dp4a chains
+      int aA[2][D], aB[2][D];
 #pragma unroll
-      for (int b = 0; b < 4; ++b) m = fmaxf(m, fabsf(load_x(a, 4 * qd + b)));
-      atomicMax(&cmax[qd / 32], __float_as_int(m));
-    }
-    __syncthreads();
-    for (int c = tid; c < nC; c += T) {
-      const float m = __int_as_float(cmax[c]);
-      int F = 0;
-      if (m > 0.f) {
-        int ex;
-        frexpf(m, &ex);  // m < 2^ex
-        F = (8 * D - 2) - ex;
-      }
-      fexp[c] = F;
-    }
-    __syncthreads();
-    // pass 2: digits, in the rotated layout read by compute(): word
-    // (step + c/4) % 8 of group c is read at step `step`, so that the 32
-    // lanes of a warp (consecutive groups) hit 32 different banks.
-    for (int qd = tid; qd < a.K / 4; qd += T) {
-      const int e = qd * 4;
-      const int c = e / 128;
-      const int tt = (e % 128) / 32;
-      const int sh = 3 - tt;
-      const int w = (e % 32) / 4;
-      const int step = (w - (c >> 2)) & 7;
-      const int F = fexp[c];
-      uint32_t dig[D];
+      for (int h = 0; h < 2; ++h)
 #pragma unroll
-      for (int d = 0; d < D; ++d) dig[d] = 0;
+        for (int d = 0; d < D; ++d) aA[h][d] = aB[h][d] = 0;
 #pragma unroll
-      for (int b = 0; b < 4; ++b) {
-        int X = __float2int_rn(ldexpf(load_x(a, e + b), F));
+      for (int h = 0; h < 2; ++h) {
+        const uint4 wv = *reinterpret_cast<const uint4*>(myrow + 32 * cc + 16 * h);
+        const uint32_t wds[4] = {wv.x, wv.y, wv.z, wv.w};
 #pragma unroll
-        for (int d = 0; d < D; ++d) {
-          const int v = ((X + 128) & 255) - 128;
-          X = (X - v) >> 8;
-          dig[d] |= uint32_t(v & 255) << (8 * b);
+        for (int j = 0; j < 4; ++j) {
+          // digits of word 4h+j: [4 shifts][D] u32, shared by the lanes on this group
+          uint32_t xw[4 * D];
+#pragma unroll
+          for (int k = 0; k < D; ++k) {
+            const uint4 q = *reinterpret_cast<const uint4*>(rec + ((4 * h + j) * 4) * D + 4 * k);
+            xw[4 * k] = q.x; xw[4 * k + 1] = q.y; xw[4 * k + 2] = q.z; xw[4 * k + 3] = q.w;
+          }
+          const uint32_t w = wds[j], w2 = w >> 2;
+          const uint32_t m0 = w & 0x03030303u, m1 = w2 & 0x03030303u;
+          const uint32_t m2 = w & 0x30303030u, m3 = w2 & 0x30303030u;
+#pragma unroll
+          for (int d = 0; d < D - 1; ++d) {  // unsigned low bytes
+            aA[h][d] = dp4a_uu(m0, xw[0 * D + d], aA[h][d]);
+            aA[h][d] = dp4a_uu(m1, xw[1 * D + d], aA[h][d]);
+            aB[h][d] = dp4a_uu(m2, xw[2 * D + d], aB[h][d]);
+            aB[h][d] = dp4a_uu(m3, xw[3 * D + d], aB[h][d]);
+          }
+          aA[h][D - 1] = dp4a_us(m0, xw[0 * D + D - 1], aA[h][D - 1]);  // signed top byte
+          aA[h][D - 1] = dp4a_us(m1, xw[1 * D + D - 1], aA[h][D - 1]);
+          aB[h][D - 1] = dp4a_us(m2, xw[2 * D + D - 1], aB[h][D - 1]);
+          aB[h][D - 1] = dp4a_us(m3, xw[3 * D + D - 1], aB[h][D - 1]);
         }
       }
+      const int* sums = reinterpret_cast<const int*>(rec + 32 * D);
+      float p = 0.f, sc = 1.f;
 #pragma unroll
-      for (int d = 0; d < D; ++d) xd[((step * 4 + sh) * D + d) * nC + c] = dig[d];
-    }
-    __syncthreads();
-    // per-group digit sums (the sum_k X_k term)
-    for (int idx = tid; idx < D * nC; idx += T) {
-      const int d = idx / nC, c = idx % nC;
-      int s = 0;
-      for (int step = 0; step < 8; ++step)
-        for (int sh = 0; sh < 4; ++sh) s = dp4a_us(0x01010101u, xd[((step * 4 + sh) * D + d) * nC + c], s);
-      sumx[d * nC + c] = s;
-    }
-    __syncthreads();
-  }
-
-  static __device__ void compute(const Args& a, const TileGeom& g, const uint8_t* tile, const uint8_t* smem, int c,
-                                 int grp, int row0, int rows, float* part) {
-    const uint32_t* xd = reinterpret_cast<const uint32_t*>(smem + g.off_pol);
-    const int* sumx = reinterpret_cast<const int*>(xd + xd_words(g.nC));
-    const int nC = g.nC;
-    const int64_t rb = g.row_bytes;
-    const uint8_t* base = tile + int64_t(grp * kI2sR) * rb + 32 * c;
-    int accA[kI2sR][D], accB[kI2sR][D];
-#pragma unroll
-    for (int r = 0; r < kI2sR; ++r)
-#pragma unroll
-      for (int d = 0; d < D; ++d) accA[r][d] = accB[r][d] = 0;
-#pragma unroll 2
-    for (int step = 0; step < 8; ++step) {
-      const int w = (step + (c >> 2)) & 7;
-      uint32_t xw[4][D];
-#pragma unroll
-      for (int sh = 0; sh < 4; ++sh)
-#pragma unroll
-        for (int d = 0; d < D; ++d) xw[sh][d] = xd[((step * 4 + sh) * D + d) * nC + c];
-      uint32_t wd[kI2sR];
-#pragma unroll
-      for (int r = 0; r < kI2sR; ++r) wd[r] = *reinterpret_cast<const uint32_t*>(base + r * rb + 4 * w);
-#pragma unroll
-      for (int r = 0; r < kI2sR; ++r) {
-        const uint32_t w2 = wd[r] >> 2;
-        const uint32_t m0 = wd[r] & 0x03030303u, m1 = w2 & 0x03030303u;
-        const uint32_t m2 = wd[r] & 0x30303030u, m3 = w2 & 0x30303030u;
-#pragma unroll
-        for (int d = 0; d < D; ++d) {
-          accA[r][d] = dp4a_us(m0, xw[0][d], accA[r][d]);
-          accA[r][d] = dp4a_us(m1, xw[1][d], accA[r][d]);
-          accB[r][d] = dp4a_us(m2, xw[2][d], accB[r][d]);
-          accB[r][d] = dp4a_us(m3, xw[3][d], accB[r][d]);
-        }
+      for (int d = 0; d < D; ++d) {
+        p += float(aA[0][d] + aA[1][d] + ((aB[0][d] + aB[1][d]) >> 4) - sums[d]) * sc;
+        sc *= 256.f;
       }
+      const float* f = reinterpret_cast<const float*>(rec + 32 * D + D);
+      yacc += (p * f[0]) * f[1];
     }
-    // 2^-F_c as two normal factors (F_c may exceed the normal exponent range)
-    const int F = sumx[D * nC + c];
-    const float scA = ldexpf(1.f, -(F / 2)), scB = ldexpf(1.f, -(F - F / 2));
-#pragma unroll
-    for (int r = 0; r < kI2sR; ++r) {
-      const int lr = grp * kI2sR + r;
-      if (lr < rows) {
-        float p = 0.f, sc = 1.f;
-#pragma unroll
-        for (int d = 0; d < D; ++d) {
-          const int t = accA[r][d] + (accB[r][d] >> 4) - sumx[d * nC + c];
-          p += float(t) * sc;
-          sc *= 256.f;
-        }
-        part[lr * nC + c] = (p * scA) * scB;
+    // lanes l and l+16 hold the two halves of row l (same order on both)
+    yacc += __shfl_xor_sync(0xffffffffu, yacc, 16);
+    __syncwarp();
+    if (i + g.stages < my_tiles) issue(i + g.stages);
+    const int row = t * kRows + r;
+    if (g.wk == 1) {
+      if (u == 0 && row < g.N) {
+        const float yv = yacc * wscale;
+        if (YB)
+          reinterpret_cast<uint16_t*>(y)[row] = f32_to_bf16_bits_rn(yv);
+        else
+          reinterpret_cast<float*>(y)[row] = yv;
+      }
+    } else {
+      float* pp = part + ((rt * 2 + (i & 1)) * g.wk) * kRows;
+      if (u == 0) pp[ks * kRows + r] = yacc;
+      // all wk warps of the tile arrive and wait, so none can run a tile ahead
+      mbar_arrive(tbar);
+      if (!mbar_wait_bounded(tbar, uint32_t(i) & 1u, g.err)) abort_flag = 1;
+      if (ks == 0 && u == 0 && row < g.N) {
+        float acc = 0.f;
+        for (int k = 0; k < g.wk; ++k) acc += pp[k * kRows + r];
+        const float yv = acc * wscale;
+        if (YB)
+          reinterpret_cast<uint16_t*>(y)[row] = f32_to_bf16_bits_rn(yv);
+        else
+          reinterpret_cast<float*>(y)[row] = yv;
       }
     }
   }
+  if (abort_flag && lane == 0) {
+    // let copies still in flight land (bounded) before the CTA exits
+    for (int j = 0; j < my_tiles && j < g.stages; ++j) mbar_wait_bounded(&full[j], 0, nullptr);
+    if (warp == 0) mbar_wait_bounded(xbar, 0, nullptr);
+  }
+}
 
-  static __device__ void finish(const Args& a, const TileGeom& g, const uint8_t* smem, const float* part, int row0,
-                                int rows, int tid, int T) {
-    const uint32_t* xd = reinterpret_cast<const uint32_t*>(smem + g.off_pol);
-    const float* consts = reinterpret_cast<const float*>(xd + xd_words(g.nC) + D * g.nC + 2 * g.nC);
-    const float s = consts[1];
-    for (int r = tid; r < rows; r += T) {
-      float acc = 0.f;
-      const float* pr = part + r * g.nC;
-      for (int c = 0; c < g.nC; ++c) acc += pr[c];
-      const float yv = acc * s;
-      if (YB)
-        reinterpret_cast<uint16_t*>(a.y)[row0 + r] = f32_to_bf16_bits_rn(yv);
-      else
-        reinterpret_cast<float*>(a.y)[row0 + r] = yv;
+template <int D>
+bool plan(Geom& g, int64_t N, int64_t K, int esize, int max_smem, int nsm) {
+  auto up = [](uint64_t v, uint64_t a) { return (v + a - 1) / a * a; };
+  g.N = int(N);
+  g.K = int(K);
+  g.nC = int(K / 128);
+  g.xbytes = int(K * esize);
+  g.ntiles = int((N + kRows - 1) / kRows);
+  // Split the groups of a tile over up to 16 warps while every warp keeps
+  // at least two groups and there are fewer than ~16 warps per SM; then put
+  // as many row tiles in a CTA as keep it at <= 16 warps without dropping
+  // below one CTA per SM.  More warps per CTA also spread the per-CTA
+  // activation preparation thinner.
+  int wk = 1;
+  while (wk < 16 && int64_t(g.ntiles) * wk < 16LL * nsm && g.nC / (wk + 1) >= 2) ++wk;
+  g.wk = wk;
+  int wr = std::max(1, 16 / wk);
+  while (wr > 1 && (g.ntiles + wr - 1) / wr < nsm) --wr;
+  g.wr = wr;
+  const int max_chunks = (g.nC + wk - 1) / wk;
+  int rs = int(up(uint64_t(max_chunks) * 32, 16));
+  if (((rs / 16) & 1) == 0) rs += 16;
+  g.rowstride = rs;
+  g.stage_bytes = uint32_t(up(uint64_t(kRows) * rs, 128));
+  const int warps = g.wk * g.wr;
+  const int64_t tiles_per_warp = (g.ntiles + int64_t(g.wr) * nsm - 1) / (int64_t(g.wr) * nsm);
+  for (int st = int(std::min<int64_t>(3, std::max<int64_t>(1, tiles_per_warp))); st >= 1; --st) {
+    uint64_t off = 0;
+    g.off_bar = uint32_t(off);
+    off = up(off + 8ull * (warps * st + 1 + g.wr), 128);
+    g.off_stage = uint32_t(off);
+    off = up(off + uint64_t(warps) * st * g.stage_bytes, 128);
+    g.off_part = uint32_t(off);
+    off = up(off + (g.wk > 1 ? 4ull * g.wr * 2 * g.wk * kRows : 0), 128);
+    g.off_x = uint32_t(off);
+    off = up(off + 4ull * g.nC * Rec<D>::kWords, 128);
+    g.off_xraw = uint32_t(off);
+    off = up(off + uint64_t(g.xbytes), 128);
+    if (off <= uint64_t(max_smem)) {
+      g.stages = st;
+      g.smem = uint32_t(off);
+      return true;
     }
   }
+  return false;
+}
+
+struct Plan {
+  Geom g;
+  int grid, threads;
+  bool ok;
 };
 
 template <int D, bool XB, bool YB>
 cudaError_t run(const uint8_t* packed, const void* x, void* y, int64_t N, int64_t K, cudaStream_t st) {
-  using Pol = I2sPolicy<D, XB, YB>;
-  const int nC = int(K / 128);
-  // threads = nC * P (<= 1024); aim for about 256 threads
-  int P = 256 / nC;
-  if (P < 1) P = 1;
-  if (P > 8) P = 8;
-  if (nC * P > 1024) return cudaErrorInvalidConfiguration;
-  TileGeom g;
-  int dev;
+  auto kern = gemv_i2s_kernel<D, XB, YB>;
+  static PlanCache<Plan> cache;
+  int dev = 0;
   cudaGetDevice(&dev);
-  int max_optin = 0;
-  cudaDeviceGetAttribute(&max_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-  // two CTAs per SM when possible
-  const uint32_t budget = uint32_t(max_optin) / 2 - 2048;
-  if (!plan_tiles(g, N, nC, P, kI2sR, 1, K / 4, 4, Pol::bytes(nC), budget) &&
-      !plan_tiles(g, N, nC, P, kI2sR, 1, K / 4, 4, Pol::bytes(nC), uint32_t(max_optin)))
-    return cudaErrorInvalidConfiguration;
-  g.err = dev_error_ptr();
-  auto kern = tiled_kernel<Pol>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(g.smem_bytes));
-  if (e != cudaSuccess) return e;
-  const int threads = (nC * P + 31) / 32 * 32;
-  int blocks_per_sm = 0;
-  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks_per_sm, kern, threads, g.smem_bytes);
-  if (blocks_per_sm < 1) blocks_per_sm = 1;
-  int grid = sm_count() * blocks_per_sm;
-  if (grid > g.ntiles) grid = g.ntiles;
-  typename Pol::Args a{packed, x, y, int(N), int(K)};
+  Plan p;
+  if (!cache.get(dev, N, K, &p)) {
+    int max_optin = 0;
+    cudaDeviceGetAttribute(&max_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    const int nsm = sm_count();
+    p.ok = plan<D>(p.g, N, K, XB ? 2 : 4, max_optin - 1024, nsm);
+    if (!p.ok) return cudaErrorInvalidConfiguration;
+    // the cap is a property of the kernel, shared by every shape: raise it to the maximum once
+    cudaError_t e = raise_smem_cap(kern, dev, max_optin - 1024);
+    if (e != cudaSuccess) return e;
+    p.threads = 32 * p.g.wk * p.g.wr;
+    int blocks_per_sm = 0;
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks_per_sm, kern, p.threads, p.g.smem);
+    if (blocks_per_sm < 1) blocks_per_sm = 1;
+    p.grid = (p.g.ntiles + p.g.wr - 1) / p.g.wr;
+    if (p.grid > nsm * blocks_per_sm) p.grid = nsm * blocks_per_sm;
+    p.g.err = dev_error_ptr();
+    cache.put(dev, N, K, p);
+  }
   const bool pdl = overlap_enabled();
-  return launch(kern, dim3(grid), dim3(threads), g.smem_bytes, st, pdl, a, g, pdl ? 1 : 0);
+  return launch(kern, dim3(p.grid), dim3(p.threads), p.g.smem, st, pdl, packed, x, y, p.g, pdl ? 1 : 0);
 }
 
 }  // namespace

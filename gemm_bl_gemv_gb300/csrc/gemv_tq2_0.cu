@@ -193,7 +193,7 @@ cudaError_t run(const uint8_t* packed, const void* x, float* y, int64_t N, int64
     return cudaErrorInvalidConfiguration;
   g.err = dev_error_ptr();
   auto kern = tiled_kernel<Pol>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(g.smem_bytes));
+  cudaError_t e = raise_smem_cap(kern, dev, max_optin);
   if (e != cudaSuccess) return e;
   const int threads = (nC * P + 31) / 32 * 32;
   int blocks_per_sm = 0;

@@ -171,8 +171,8 @@ bl_status bl_quantize_act_absmax_int8(const void* x, bl_dtype xt, int64_t M, int
  * rounded to bf16 if asked.  For activations without extreme in-group
  * outliers the error is within 1e-5 (fp32 output) / 2e-2 (bf16 output) of
  * |scale| * sum_j |w[i,j]| |x[j]| + |y[i]|.
- * Requires K % 128 == 0, N >= 1; `packed` 16-byte aligned; x and y aligned
- * to their element size.  Non-finite x gives unspecified y.
+ * Requires K % 128 == 0, K <= 32768, N >= 1; `packed` 16-byte aligned; x
+ * and y aligned to their element size.  Non-finite x gives unspecified y.
  */
 bl_status bl_gemv_i2s(const uint8_t* packed, const void* x, bl_dtype xt, void* y, bl_dtype yt, int64_t N, int64_t K,
                       bl_stream_t stream);
