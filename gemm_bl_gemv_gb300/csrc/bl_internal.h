@@ -90,6 +90,10 @@ cudaError_t launch_gemv_tq2_0(const uint8_t* packed, const void* x, bl_dtype xt,
 cudaError_t launch_gemm_w1a8(const int8_t* q, const float* sc, const int32_t* wq, const uint16_t* ws,
                              const uint16_t* bias, int64_t M, int64_t N, int64_t K, int group, uint16_t* y,
                              int32_t* dots, cudaStream_t s);
+bool w1a8_rows_applicable(int64_t M, int64_t K, int G);
+cudaError_t launch_gemm_w1a8_rows(const int8_t* q, const float* s, const int32_t* wq, const uint16_t* ws,
+                                  const uint16_t* bias, int64_t M, int64_t N, int64_t K, int group, uint16_t* y,
+                                  int32_t* dots, cudaStream_t st);
 cudaError_t launch_gemm_i2s_int8_simt(const int8_t* q, const float* sc, const uint8_t* packed, int64_t M, int64_t N,
                                       int64_t K, float* y, int32_t* acc, cudaStream_t s);
 cudaError_t launch_gemm_i2s_int8(const int8_t* q, const float* sc, const uint8_t* packed, int64_t M, int64_t N,

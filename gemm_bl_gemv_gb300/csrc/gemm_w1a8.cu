@@ -1,5 +1,6 @@
-// W1A8 product for 1 <= M <= 8 tokens ("binary-gemm" card, sections "API"
-// binary_gemm and "Method"):
+// W1A8 product for 1 <= M <= 8 tokens, tiled kernel for shapes the
+// lane-per-row kernel (gemm_w1a8_rows.cu) does not take ("binary-gemm"
+// card, sections "API" binary_gemm and "Method"):
 //   dot[m,n,g] = sum_{k in g} w[n,k] q[m,k]     (exact)
 //   y[m,n]     = bf16( s[m] * sum_g ws[n,g] * dot[m,n,g] + bias[n] )
 // with the card's identity dot(w, a) = 2 * sum_{b=1} a - sum a (stored bit
@@ -214,6 +215,10 @@ cudaError_t dispatch(int M, const int8_t* q, const float* s, const int32_t* wq, 
 cudaError_t launch_gemm_w1a8(const int8_t* q, const float* s, const int32_t* wq, const uint16_t* ws,
                              const uint16_t* bias, int64_t M, int64_t N, int64_t K, int group, uint16_t* y,
                              int32_t* dots, cudaStream_t st) {
+  if (w1a8_rows_applicable(M, K, group)) {
+    const cudaError_t e = launch_gemm_w1a8_rows(q, s, wq, ws, bias, M, N, K, group, y, dots, st);
+    if (e != cudaErrorNotSupported) return e;
+  }
   if (dots) return dispatch<true>(int(M), q, s, wq, ws, bias, N, K, group, y, dots, st);
   return dispatch<false>(int(M), q, s, wq, ws, bias, N, K, group, y, dots, st);
 }

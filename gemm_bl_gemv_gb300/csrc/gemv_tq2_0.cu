@@ -1,209 +1,319 @@
 // TQ2_0 GEMV, one token ("Hesper/Quantization/TQ2_0", section "TQ2_0 Format"):
 //   y[n] = sum_b d[n,b] * sum_{j<256} w[n,256b+j] x[256b+j]
-// A block is 64 code bytes then its fp16 scale: 66 bytes, so blocks of odd
-// index inside a tile start 2 bytes past a 4-byte boundary; their code words
-// are assembled from two aligned shared-memory words with a funnel shift.
+//
+// Work decomposition.  A warp owns a tile of 8 consecutive rows; four lanes
+// work on each row and take every fourth 256-element block; their sums are
+// added with two shuffles.  A tile is contiguous in memory (8 * 66 bytes per
+// block, always a multiple of 16), so one thread bulk-copies it
+// (cp.async.bulk) into a ring buffer of the warp.  Blocks of odd index start
+// 2 bytes past a 4-byte boundary; their code words are assembled from two
+// aligned shared-memory words with a funnel shift.
 //
 // Decode.  Element j of a block sits in byte j/4 at shift 2*(j%4) with codes
 // 00 -> 0, 01 -> +1, 11 -> -1.  XOR with 0b01 maps the codes to
-// t = 1 - w in {1, 0, 2}, so sum_j w_j X_j = sum_j X_j - sum_j t_j X_j and
-// the same byte-mask + dp4a decode as i2_s applies (classes = shift 0,2,4,6,
-// i.e. elements 16i+4b+{0,1,2,3} of word i, byte b).  The per-block integer
-// sum is converted to fp32 once and multiplied by the block scale.
+// t = 1 - w in {1, 0, 2}, so sum_j w_j X_j = sum_j X_j - sum_j t_j X_j and a
+// byte-mask + dp4a decode applies: in word i of a block, byte b holds
+// elements 16i+4b+{0,1,2,3} at shifts 0,2,4,6:
+//   shift 0: w & 0x03030303, shift 2: (w >> 2) & 0x03030303,
+//   shift 4: w & 0x30303030 (x16), shift 6: (w >> 2) & 0x30303030 (x16).
+// The per-block integer sum is converted to fp32 once and multiplied by the
+// block scale.
 //
-// Activations: exact fixed-point digits as in the i2_s GEMV, with one
-// exponent per 256-element block (D = 4 for fp32 x, D = 3 for bf16 x).
+// Activations: once per CTA, exact fixed-point integers with one exponent per
+// 256-element block (as in the i2_s GEMV: D = 4 bytes for fp32 x, D = 3 for
+// bf16 x, two's complement, signed top byte), read by broadcast.
+#include <algorithm>
+
+#include "bl_device.cuh"
 #include "bl_internal.h"
-#include "gemv_tiled.cuh"
 
 namespace bl {
 namespace {
 
-constexpr int kTqR = 4;
+constexpr int kRows = 8;  // rows per warp tile (four lanes per row)
+
+struct Geom {
+  int N, K, nb;          // rows, columns, 256-element blocks per row
+  int wpb, stages, ntiles;
+  int64_t row_bytes;     // nb * 66
+  uint32_t stage_bytes;  // kRows * row_bytes (+4) rounded up to 128
+  uint32_t off_bar, off_stage, off_rec, off_xraw, smem;
+  int xbytes;
+  unsigned int* err;
+};
+
+// Per-block activation record: [16 words][4 shifts][D] u32, D digit sums,
+// two fp32 factors whose product is 2^-F_b, padding to 16 bytes.
+template <int D>
+struct Rec {
+  static constexpr int kWords = (64 * D + D + 2 + 3) / 4 * 4;
+};
 
 template <int D, bool XB>
-struct Tq2Policy {
-  static constexpr int kMaxThreads = 1024;
-  struct Args {
-    const uint8_t* packed;
-    const void* x;
-    float* y;
-    int N, K;
+__device__ __forceinline__ void prepare_x(const uint8_t* xraw, int nb, uint32_t* xrec, int warp, int nwarps,
+                                          int lane) {
+  constexpr int RW = Rec<D>::kWords;
+  for (int c = warp; c < nb; c += nwarps) {
+    // lane l holds elements 8l..8l+7 of block c: word i = l/2, bytes 2(l&1), 2(l&1)+1
+    float v[8];
+    const int e0 = c * 256 + 8 * lane;
+    if (XB) {
+      const uint4 q = *reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(xraw) + e0);
+      const uint32_t h[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        v[2 * k] = __uint_as_float(h[k] << 16);
+        v[2 * k + 1] = __uint_as_float(h[k] & 0xFFFF0000u);
+      }
+    } else {
+      const float4 a = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(xraw) + e0);
+      const float4 b = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(xraw) + e0 + 4);
+      v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+    }
+    float mm = 0.f;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) mm = fmaxf(mm, fabsf(v[k]));
+    const float m = __uint_as_float(redux_max_u32(__float_as_uint(mm)));
+    const int F = m > 0.f ? (8 * D - 1) - exponent_of(m) : 0;
+    const int fa = F / 2, fb = F - fa;
+    const float sA = exp2i(fa), sB = exp2i(fb);
+    int X[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      constexpr int kLim = int((1u << (8 * D - 1)) - 1u);
+      X[k] = max(-kLim, min(kLim, __float2int_rn(__fmul_rn(__fmul_rn(v[k], sA), sB))));
+    }
+    uint32_t* rec = xrec + c * RW;
+    const int i = lane >> 1, half = lane & 1;
+#pragma unroll
+    for (int d = 0; d < D; ++d) {
+      const uint32_t sel = uint32_t(d) | (uint32_t(d + 4) << 4);
+      int dsum = 0;
+#pragma unroll
+      for (int sh = 0; sh < 4; ++sh) {
+        // this lane's two bytes of word i, shift class sh: elements 8*half+sh and 8*half+4+sh
+        const uint32_t mine = __byte_perm(uint32_t(X[sh]), uint32_t(X[4 + sh]), sel);  // low half used
+        const uint32_t other = __shfl_xor_sync(0xffffffffu, mine, 1);
+        const uint32_t word = half ? __byte_perm(other, mine, 0x5410) : __byte_perm(mine, other, 0x5410);
+        if (half == 0) rec[(i * 4 + sh) * D + d] = word;
+        dsum = (d == D - 1) ? dp4a_us(0x00000101u, mine, dsum) : dp4a_uu(0x00000101u, mine, dsum);
+      }
+      const int s = redux_add(dsum);
+      if (lane == 0) reinterpret_cast<int*>(rec)[64 * D + d] = s;
+    }
+    if (lane == 0) {
+      reinterpret_cast<float*>(rec)[64 * D + D] = exp2i(-fa);
+      reinterpret_cast<float*>(rec)[64 * D + D + 1] = exp2i(-fb);
+    }
+  }
+}
+
+template <int D, bool XB>
+__global__ void __launch_bounds__(256) gemv_tq2_0_kernel(const uint8_t* __restrict__ packed,
+                                                         const void* __restrict__ x, float* __restrict__ y, Geom g,
+                                                         int early_weights) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  constexpr int RW = Rec<D>::kWords;
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const int nwarps = blockDim.x >> 5;
+  const int r = lane & (kRows - 1), v = lane >> 3;  // row of the tile, block residue
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + g.off_bar) + warp * g.stages;
+  uint64_t* xbar = reinterpret_cast<uint64_t*>(smem + g.off_bar) + nwarps * g.stages;
+  uint8_t* ring = smem + g.off_stage + size_t(warp) * g.stages * g.stage_bytes;
+  uint32_t* xrec = reinterpret_cast<uint32_t*>(smem + g.off_rec);
+  uint8_t* xraw = smem + g.off_xraw;
+  __shared__ int abort_flag;
+
+  const int tile_stride = int(gridDim.x) * nwarps;
+  const int first = int(blockIdx.x) * nwarps + warp;
+  const int my_tiles = first < g.ntiles ? (g.ntiles - 1 - first) / tile_stride + 1 : 0;
+
+  auto issue = [&](int i) {  // lane 0 only
+    const int t = first + i * tile_stride;
+    const int st = i % g.stages;
+    const int nrows = min(kRows, g.N - t * kRows);
+    const uint64_t bytes = uint64_t(nrows) * uint64_t(g.row_bytes);
+    const uint32_t b16 = uint32_t(bytes & ~uint64_t(15));
+    uint8_t* dst = ring + size_t(st) * g.stage_bytes;
+    const uint8_t* src = packed + int64_t(t) * kRows * g.row_bytes;
+    // a last tile that is not a multiple of 16 bytes: its tail goes by plain loads
+    for (uint32_t k = b16; k < uint32_t(bytes); ++k) dst[k] = src[k];
+    mbar_arrive_expect_tx(&full[st], b16);
+    if (b16) bulk_g2s(dst, src, b16, &full[st], policy_evict_first());
   };
-  // policy area: [xd: 16 words x 4 classes x D x nC u32][sumx: D x nC][fexp: nC][cmax: nC]
-  static __host__ __device__ uint32_t xd_words(int nC) { return 16u * 4u * D * nC; }
-  static __host__ __device__ uint32_t bytes(int nC) { return (xd_words(nC) + D * nC + 2 * nC + 8) * 4; }
 
-  static __device__ const uint8_t* weights(const Args& a) { return a.packed; }
-  static __device__ const uint8_t* aux(const Args&) { return nullptr; }
-
-  static __device__ float load_x(const Args& a, int e) {
-    if (XB) return bf16_bits_to_f32(reinterpret_cast<const uint16_t*>(a.x)[e]);
-    return reinterpret_cast<const float*>(a.x)[e];
+  if (lane == 0)
+    for (int st = 0; st < g.stages; ++st) mbar_init(&full[st], 1);
+  if (threadIdx.x == 0) {
+    mbar_init(xbar, 1);
+    abort_flag = 0;
   }
+  fence_barrier_init();
+  __syncthreads();
+  const int npre = min(my_tiles, g.stages);
+  if (early_weights && lane == 0)
+    for (int i = 0; i < npre; ++i) issue(i);
+  pdl_wait();
+  const bool x_bulk = (reinterpret_cast<uintptr_t>(x) & 15) == 0;
+  if (threadIdx.x == 0 && x_bulk) {
+    mbar_arrive_expect_tx(xbar, uint32_t(g.xbytes));
+    bulk_g2s(xraw, x, uint32_t(g.xbytes), xbar, policy_evict_first());
+  }
+  if (!early_weights && lane == 0)
+    for (int i = 0; i < npre; ++i) issue(i);
+  if (x_bulk) {
+    if (!mbar_wait_bounded(xbar, 0, g.err)) abort_flag = 1;
+  } else {
+    for (int k = threadIdx.x; k < g.xbytes / 2; k += blockDim.x)
+      reinterpret_cast<uint16_t*>(xraw)[k] = reinterpret_cast<const uint16_t*>(x)[k];
+    __syncthreads();
+  }
+  prepare_x<D, XB>(xraw, g.nb, xrec, warp, nwarps, lane);
+  __syncthreads();
+  pdl_launch_dependents();
 
-  static __device__ void prepare(const Args& a, const TileGeom& g, uint8_t* smem, int tid, int T) {
-    const int nC = g.nC;
-    uint32_t* xd = reinterpret_cast<uint32_t*>(smem + g.off_pol);
-    int* sumx = reinterpret_cast<int*>(xd + xd_words(nC));
-    int* fexp = sumx + D * nC;
-    int* cmax = fexp + nC;
-    for (int c = tid; c < nC; c += T) cmax[c] = 0;
-    __syncthreads();
-    for (int idx = tid; idx < nC * 16; idx += T) {
-      float m = 0.f;
-      for (int j = 0; j < 16; ++j) m = fmaxf(m, fabsf(load_x(a, 16 * idx + j)));
-      atomicMax(&cmax[idx / 16], __float_as_int(m));
-    }
-    __syncthreads();
-    for (int c = tid; c < nC; c += T) {
-      const float m = __int_as_float(cmax[c]);
-      int F = 0;
-      if (m > 0.f) {
-        int ex;
-        frexpf(m, &ex);
-        F = (8 * D - 2) - ex;
-      }
-      fexp[c] = F;
-    }
-    __syncthreads();
-    // one (block c, word i) per iteration: elements 256c + 16i + 0..15
-    for (int idx = tid; idx < nC * 16; idx += T) {
-      const int c = idx / 16, i = idx % 16;
-      const int F = fexp[c];
-      uint32_t dig[4][D];
+  for (int i = 0; i < my_tiles; ++i) {
+    const int st = i % g.stages;
+    const int t = first + i * tile_stride;
+    if (!abort_flag && !mbar_wait_bounded(&full[st], uint32_t(i / g.stages) & 1u, g.err)) abort_flag = 1;
+    __syncwarp();
+    const uint8_t* buf = ring + size_t(st) * g.stage_bytes;
+    const uint32_t row_off = uint32_t(r * g.row_bytes);
+    float yacc = 0.f;
+    for (int b = v; b < g.nb; b += 4) {
+      const uint32_t* rec = xrec + b * RW;
+      int aA[2][D], aB[2][D];
 #pragma unroll
-      for (int sh = 0; sh < 4; ++sh)
+      for (int h = 0; h < 2; ++h)
 #pragma unroll
-        for (int d = 0; d < D; ++d) dig[sh][d] = 0;
+        for (int d = 0; d < D; ++d) aA[h][d] = aB[h][d] = 0;
+      // block start inside the buffer, and its offset from a 4-byte boundary (0 or 2)
+      const uint32_t boff = row_off + 66u * uint32_t(b);
+      const uint32_t fs = (boff & 3u) * 8u;
+      const uint32_t* aw = reinterpret_cast<const uint32_t*>(buf + (boff & ~3u));
+      uint32_t nxt = aw[0];
+#pragma unroll 4
+      for (int wi = 0; wi < 16; ++wi) {
+        const uint32_t cur = nxt;
+        nxt = aw[wi + 1];
+        const uint32_t w = __funnelshift_r(cur, nxt, fs) ^ 0x55555555u;
+        uint32_t xw[4 * D];
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        int X = __float2int_rn(ldexpf(load_x(a, 256 * c + 16 * i + j), F));
-        const int b = j >> 2, sh = j & 3;
-#pragma unroll
-        for (int d = 0; d < D; ++d) {
-          const int v = ((X + 128) & 255) - 128;
-          X = (X - v) >> 8;
-          dig[sh][d] |= uint32_t(v & 255) << (8 * b);
+        for (int k = 0; k < D; ++k) {
+          const uint4 q = *reinterpret_cast<const uint4*>(rec + (wi * 4) * D + 4 * k);
+          xw[4 * k] = q.x; xw[4 * k + 1] = q.y; xw[4 * k + 2] = q.z; xw[4 * k + 3] = q.w;
         }
-      }
+        const uint32_t w2 = w >> 2;
+        const uint32_t m0 = w & 0x03030303u, m1 = w2 & 0x03030303u;
+        const uint32_t m2 = w & 0x30303030u, m3 = w2 & 0x30303030u;
+        const int h = wi & 1;
 #pragma unroll
-      for (int sh = 0; sh < 4; ++sh)
-#pragma unroll
-        for (int d = 0; d < D; ++d) xd[((i * 4 + sh) * D + d) * nC + c] = dig[sh][d];
-    }
-    __syncthreads();
-    for (int idx = tid; idx < D * nC; idx += T) {
-      const int d = idx / nC, c = idx % nC;
-      int s = 0;
-      for (int i = 0; i < 16; ++i)
-        for (int sh = 0; sh < 4; ++sh) s = dp4a_us(0x01010101u, xd[((i * 4 + sh) * D + d) * nC + c], s);
-      sumx[d * nC + c] = s;
-    }
-    __syncthreads();
-  }
-
-  static __device__ void compute(const Args& a, const TileGeom& g, const uint8_t* tile, const uint8_t* smem, int c,
-                                 int grp, int row0, int rows, float* part) {
-    const uint32_t* xd = reinterpret_cast<const uint32_t*>(smem + g.off_pol);
-    const int* sumx = reinterpret_cast<const int*>(xd + xd_words(g.nC));
-    const int nC = g.nC;
-    const int64_t rb = g.row_bytes;
-    int accA[kTqR][D], accB[kTqR][D];
-#pragma unroll
-    for (int r = 0; r < kTqR; ++r)
-#pragma unroll
-      for (int d = 0; d < D; ++d) accA[r][d] = accB[r][d] = 0;
-    // byte offset of block c of row (grp*R + r) inside the tile
-    uint32_t boff[kTqR];
-#pragma unroll
-    for (int r = 0; r < kTqR; ++r) boff[r] = uint32_t((grp * kTqR + r) * rb + 66 * c);
-#pragma unroll 2
-    for (int i = 0; i < 16; ++i) {
-      uint32_t xw[4][D];
-#pragma unroll
-      for (int sh = 0; sh < 4; ++sh)
-#pragma unroll
-        for (int d = 0; d < D; ++d) xw[sh][d] = xd[((i * 4 + sh) * D + d) * nC + c];
-#pragma unroll
-      for (int r = 0; r < kTqR; ++r) {
-        const uint32_t addr = boff[r] + 4 * i;
-        const uint32_t* p = reinterpret_cast<const uint32_t*>(tile + (addr & ~3u));
-        const uint32_t wd = __funnelshift_r(p[0], p[1], (addr & 3u) * 8) ^ 0x55555555u;
-        const uint32_t w2 = wd >> 2;
-        const uint32_t m0 = wd & 0x03030303u, m1 = w2 & 0x03030303u;
-        const uint32_t m2 = wd & 0x30303030u, m3 = w2 & 0x30303030u;
-#pragma unroll
-        for (int d = 0; d < D; ++d) {
-          accA[r][d] = dp4a_us(m0, xw[0][d], accA[r][d]);
-          accA[r][d] = dp4a_us(m1, xw[1][d], accA[r][d]);
-          accB[r][d] = dp4a_us(m2, xw[2][d], accB[r][d]);
-          accB[r][d] = dp4a_us(m3, xw[3][d], accB[r][d]);
+        for (int d = 0; d < D - 1; ++d) {
+          aA[h][d] = dp4a_uu(m0, xw[0 * D + d], aA[h][d]);
+          aA[h][d] = dp4a_uu(m1, xw[1 * D + d], aA[h][d]);
+          aB[h][d] = dp4a_uu(m2, xw[2 * D + d], aB[h][d]);
+          aB[h][d] = dp4a_uu(m3, xw[3 * D + d], aB[h][d]);
         }
+        aA[h][D - 1] = dp4a_us(m0, xw[0 * D + D - 1], aA[h][D - 1]);
+        aA[h][D - 1] = dp4a_us(m1, xw[1 * D + D - 1], aA[h][D - 1]);
+        aB[h][D - 1] = dp4a_us(m2, xw[2 * D + D - 1], aB[h][D - 1]);
+        aB[h][D - 1] = dp4a_us(m3, xw[3 * D + D - 1], aB[h][D - 1]);
       }
-    }
-    const int F = sumx[D * nC + c];
-    const float scA = ldexpf(1.f, -(F / 2)), scB = ldexpf(1.f, -(F - F / 2));
+      const int* sums = reinterpret_cast<const int*>(rec + 64 * D);
+      float p = 0.f, sc = 1.f;
 #pragma unroll
-    for (int r = 0; r < kTqR; ++r) {
-      const int lr = grp * kTqR + r;
-      if (lr < rows) {
-        float p = 0.f, sc = 1.f;
-#pragma unroll
-        for (int d = 0; d < D; ++d) {
-          const int t = sumx[d * nC + c] - (accA[r][d] + (accB[r][d] >> 4));
-          p += float(t) * sc;
-          sc *= 256.f;
-        }
-        const uint16_t dbits = *reinterpret_cast<const uint16_t*>(tile + boff[r] + 64);
-        part[lr * nC + c] = __half2float(__ushort_as_half(dbits)) * ((p * scA) * scB);
+      for (int d = 0; d < D; ++d) {
+        p += float(sums[d] - (aA[0][d] + aA[1][d] + ((aB[0][d] + aB[1][d]) >> 4))) * sc;
+        sc *= 256.f;
       }
+      const float* f = reinterpret_cast<const float*>(rec + 64 * D + D);
+      const float dsc = __half2float(__ushort_as_half(*reinterpret_cast<const uint16_t*>(buf + boff + 64)));
+      yacc += dsc * ((p * f[0]) * f[1]);
     }
+    // the four lanes of a row hold blocks b = v (mod 4); add them (same order on all four)
+    yacc += __shfl_xor_sync(0xffffffffu, yacc, 8);
+    yacc += __shfl_xor_sync(0xffffffffu, yacc, 16);
+    __syncwarp();
+    if (lane == 0 && i + g.stages < my_tiles) issue(i + g.stages);
+    const int row = t * kRows + r;
+    if (v == 0 && row < g.N) y[row] = yacc;
   }
+  if (abort_flag && lane == 0) {
+    for (int j = 0; j < my_tiles && j < g.stages; ++j) mbar_wait_bounded(&full[j], 0, nullptr);
+    if (warp == 0) mbar_wait_bounded(xbar, 0, nullptr);
+  }
+}
 
-  static __device__ void finish(const Args& a, const TileGeom& g, const uint8_t* smem, const float* part, int row0,
-                                int rows, int tid, int T) {
-    for (int r = tid; r < rows; r += T) {
-      float acc = 0.f;
-      const float* pr = part + r * g.nC;
-      for (int c = 0; c < g.nC; ++c) acc += pr[c];
-      a.y[row0 + r] = acc;
+template <int D>
+bool plan(Geom& g, int64_t N, int64_t K, int esize, int max_smem, int nsm) {
+  auto up = [](uint64_t v, uint64_t a) { return (v + a - 1) / a * a; };
+  g.N = int(N);
+  g.K = int(K);
+  g.nb = int(K / 256);
+  g.row_bytes = int64_t(g.nb) * 66;
+  g.xbytes = int(K * esize);
+  g.ntiles = int((N + kRows - 1) / kRows);
+  // + 4 bytes so the funnel-shift read of the last word stays inside the buffer
+  g.stage_bytes = uint32_t(up(uint64_t(kRows) * g.row_bytes + 4, 128));
+  // warps per CTA: up to 8, fewer when tiles are few
+  int wpb = 8;
+  while (wpb > 1 && int64_t(g.ntiles) < int64_t(wpb) * nsm / 2) wpb /= 2;
+  g.wpb = wpb;
+  const int64_t tiles_per_warp = (g.ntiles + int64_t(wpb) * nsm - 1) / (int64_t(wpb) * nsm);
+  // prefer two CTAs per SM: the deepest ring that fits half the shared memory, else the whole
+  for (int half = 1; half >= 0; --half) {
+    const uint64_t lim = half ? uint64_t(max_smem) / 2 - 1024 : uint64_t(max_smem);
+    for (int st = int(std::min<int64_t>(3, std::max<int64_t>(1, tiles_per_warp))); st >= 1; --st) {
+      uint64_t off = 0;
+      g.off_bar = uint32_t(off);
+      off = up(off + 8ull * (wpb * st + 1), 128);
+      g.off_stage = uint32_t(off);
+      off = up(off + uint64_t(wpb) * st * g.stage_bytes, 128);
+      g.off_rec = uint32_t(off);
+      off = up(off + 4ull * g.nb * Rec<D>::kWords, 128);
+      g.off_xraw = uint32_t(off);
+      off = up(off + uint64_t(g.xbytes), 128);
+      if (off <= lim) {
+        g.stages = st;
+        g.smem = uint32_t(off);
+        return true;
+      }
     }
   }
+  return false;
+}
+
+struct Plan {
+  Geom g;
+  int grid, threads;
 };
 
 template <int D, bool XB>
 cudaError_t run(const uint8_t* packed, const void* x, float* y, int64_t N, int64_t K, cudaStream_t st) {
-  using Pol = Tq2Policy<D, XB>;
-  const int nC = int(K / 256);
-  int P = 256 / nC;
-  if (P < 1) P = 1;
-  if (P > 8) P = 8;
-  // tile bytes must be a multiple of 16 for the bulk copy: TR * nC * 66 % 16 == 0
-  while ((P * kTqR * nC * 66) % 16 != 0) ++P;
-  if (nC * P > 1024) return cudaErrorInvalidConfiguration;
-  TileGeom g;
-  int dev;
+  auto kern = gemv_tq2_0_kernel<D, XB>;
+  static PlanCache<Plan> cache;
+  int dev = 0;
   cudaGetDevice(&dev);
-  int max_optin = 0;
-  cudaDeviceGetAttribute(&max_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-  const uint32_t budget = uint32_t(max_optin) / 2 - 2048;
-  if (!plan_tiles(g, N, nC, P, kTqR, 1, int64_t(nC) * 66, 4, Pol::bytes(nC), budget) &&
-      !plan_tiles(g, N, nC, P, kTqR, 1, int64_t(nC) * 66, 4, Pol::bytes(nC), uint32_t(max_optin)))
-    return cudaErrorInvalidConfiguration;
-  g.err = dev_error_ptr();
-  auto kern = tiled_kernel<Pol>;
-  cudaError_t e = raise_smem_cap(kern, dev, max_optin);
-  if (e != cudaSuccess) return e;
-  const int threads = (nC * P + 31) / 32 * 32;
-  int blocks_per_sm = 0;
-  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks_per_sm, kern, threads, g.smem_bytes);
-  if (blocks_per_sm < 1) blocks_per_sm = 1;
-  int grid = sm_count() * blocks_per_sm;
-  if (grid > g.ntiles) grid = g.ntiles;
-  typename Pol::Args a{packed, x, y, int(N), int(K)};
+  Plan p;
+  if (!cache.get(dev, N, K, &p)) {
+    int max_optin = 0;
+    cudaDeviceGetAttribute(&max_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    const int nsm = sm_count();
+    if (!plan<D>(p.g, N, K, XB ? 2 : 4, max_optin - 1024, nsm)) return cudaErrorInvalidConfiguration;
+    cudaError_t e = raise_smem_cap(kern, dev, max_optin - 1024);
+    if (e != cudaSuccess) return e;
+    p.threads = 32 * p.g.wpb;
+    int bps = 0;
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bps, kern, p.threads, p.g.smem);
+    if (bps < 1) bps = 1;
+    p.grid = (p.g.ntiles + p.g.wpb - 1) / p.g.wpb;
+    if (p.grid > nsm * bps) p.grid = nsm * bps;
+    p.g.err = dev_error_ptr();
+    cache.put(dev, N, K, p);
+  }
   const bool pdl = overlap_enabled();
-  return launch(kern, dim3(grid), dim3(threads), g.smem_bytes, st, pdl, a, g, pdl ? 1 : 0);
+  return launch(kern, dim3(p.grid), dim3(p.threads), p.g.smem, st, pdl, packed, x, y, p.g, pdl ? 1 : 0);
 }
 
 }  // namespace
