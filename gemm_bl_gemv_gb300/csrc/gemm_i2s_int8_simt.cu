@@ -1,8 +1,8 @@
 // i2_s x int8 product on the CUDA cores (exact int32 accumulation with dp4a).
 //   acc[m,n] = sum_k q[m,k] w[n,k];   y[m,n] = f32(acc) * s[m] * scale
 // ("Hesper/Layers/BitLinear", "BitLinear Mathematics", with int8 activations
-// as produced by the per-token absmax quantizer).  Used for shapes the
-// tensor-core kernel does not take and as its cross-check.
+// as produced by the per-token absmax quantizer).  Used for small batches
+// (M < 64), where a 128-row tensor-core tile would be mostly padding.
 #include "bl_device.cuh"
 #include "bl_internal.h"
 
@@ -107,11 +107,6 @@ cudaError_t launch_gemm_i2s_int8_simt(const int8_t* q, const float* sc, const ui
   dim3 grid(unsigned((N + kBN - 1) / kBN), unsigned((M + kBM - 1) / kBM));
   return launch(gemm_i2s_int8_simt_kernel, grid, dim3(256), 0, s, overlap_enabled(), q, sc, packed, int(M), int(N),
                 int(K), y, acc);
-}
-
-cudaError_t launch_gemm_i2s_int8(const int8_t* q, const float* sc, const uint8_t* packed, int64_t M, int64_t N,
-                                 int64_t K, float* y, int32_t* acc, cudaStream_t s) {
-  return launch_gemm_i2s_int8_simt(q, sc, packed, M, N, K, y, acc, s);
 }
 
 }  // namespace bl
