@@ -207,7 +207,7 @@ def time_graph(torch, dist, body, steps, warmup, graph_steps, stream):
 def kernel_source_hash():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "gemm_bl_gemv_gb300", "csrc")
-    for f in ("gemv_i2s.cu", "gemv_tiled.cuh", "bl_device.cuh"):
+    for f in ("gemv_i2s.cu", "bl_device.cuh", "bl_internal.h"):
         h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:16]
 
@@ -336,7 +336,7 @@ def bench_ours(args, dist):
                        "launch": "CUDA graph of %d steps, programmatic dependent launch" % gs},
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
                          "frac": round(achieved / hbm, 4), "traffic": profiled_traffic(),
-                         "kernel": "tiled_kernel<I2sPolicy<3,bf16,bf16>>",
+                         "kernel": "gemv_i2s_kernel<3, bf16 x, bf16 y>",
                          "algorithmic_bytes_per_launch": mlp_algorithmic_bytes_per_launch(),
                          "peak_source": peak_src + " copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"},
             "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,

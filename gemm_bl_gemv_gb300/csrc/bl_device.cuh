@@ -129,17 +129,10 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
-// One-instruction warp reductions (redux.sync).
-__device__ __forceinline__ int redux_add(int v) {
-  int r;
-  asm volatile("redux.sync.add.s32 %0, %1, 0xffffffff;" : "=r"(r) : "r"(v));
-  return r;
-}
-__device__ __forceinline__ uint32_t redux_max_u32(uint32_t v) {
-  uint32_t r;
-  asm volatile("redux.sync.max.u32 %0, %1, 0xffffffff;" : "=r"(r) : "r"(v));
-  return r;
-}
+// One-instruction warp reductions (redux.sync), whole warp.  The builtins
+// leave the compiler free to interleave independent reductions.
+__device__ __forceinline__ int redux_add(int v) { return __reduce_add_sync(0xffffffffu, v); }
+__device__ __forceinline__ uint32_t redux_max_u32(uint32_t v) { return __reduce_max_sync(0xffffffffu, v); }
 
 __device__ __forceinline__ int warp_sum_int(int v) {
 #pragma unroll

@@ -2,18 +2,30 @@
 // ("Hesper/Layers/BitLinear", sections "i2_s Packing Format" and
 // "BitLinear Mathematics").
 //
-// Work decomposition.  A warp owns a tile of 16 rows: lanes l and l+16 both
-// work on row l of the tile and take alternate 128-element groups of the
-// warp's group range; their sums are added with one shuffle.  When rows are
-// few the group range of a tile is split over `wk` warps of the CTA and
-// their row sums are added in warp order.  Each row's slice is bulk-copied
-// (cp.async.bulk) into a shared-memory row whose stride is an odd number of
-// 16-byte units, so the 128-bit reads of every 8-lane phase hit distinct
-// banks.  The activation digits of a group are read by broadcast (at most
-// two addresses per instruction).  Row tiles of a warp stream through a ring
-// of `stages` buffers completed by mbarriers (bounded waits).  The
-// activation vector itself arrives by one bulk copy issued right after the
-// wait on the previous kernel.
+// Work decomposition.  The grid has one CTA per SM (fewer when N is small)
+// and CTA c takes an equal contiguous range of rows (N/grid, rounded up for
+// the first N % grid CTAs), so no SM holds more than one row above its
+// share.  A CTA covers its rows with tiles of 16 (the last may be partial);
+// when only a few rows (<= kExtraMax) are left over they are taken one row
+// at a time instead, which costs about 1/16 of a tile per row.  The unit of
+// work is one 128-element group of a tile (or of a single row); the tile
+// units of the CTA are split evenly over its 16 warps, and so are the
+// single-row units.  In a tile, lanes l and l+16 both work on row l and
+// take alternate groups; their sums meet with one shuffle.  For a single
+// row, lane (w, t) takes word w of each group and the codes of shift class
+// t (its integer sum over its 4 elements is exact), and the warp adds its
+// lanes at the end.  A tile or row cut between
+// warps is summed in warp order in shared memory.  Nothing leaves the CTA
+// before it is final, so results do not depend on timing.
+//
+// Staging.  A warp's units stream through a ring of `stages` buffers, one
+// chunk (up to S groups of one tile or row) per buffer: each row's bytes
+// arrive by a bulk copy (cp.async.bulk) into a shared-memory row whose
+// stride is an odd number of 16-byte units, so the 128-bit reads of an
+// 8-lane phase hit distinct banks; buffers complete on mbarriers (bounded
+// waits).  With programmatic dependent launch the first chunks are
+// requested before the wait on the previous kernel, since the weights do
+// not depend on it.
 //
 // Decode.  A 32-bit word of a group holds bytes p..p+3; bits (7-2t):(6-2t)
 // of byte p are the code of element 32t+p.  Byte masks of the codes:
@@ -31,7 +43,10 @@
 // unsigned low bytes u_d and a signed top byte).  D = 4 for fp32 input
 // (fp32 values within 7 binades of the group maximum are carried exactly,
 // smaller ones with absolute error <= 2^-32 * 2^ceil(log2 max)), D = 3 for
-// bf16 input (exact within 15 binades).  Products and sums over a group are
+// bf16 input with fp32 output (exact within 15 binades) and D = 2 for bf16
+// input and output (exact within 7 binades, error <= 2^-16 * 2^ceil(log2
+// max) below that: far under the output's own bf16 rounding, for a third
+// fewer dp4a).  Products and sums over a group are
 // exact integers; each group sum is converted to fp32 once, scaled by
 // 2^-F_g and added.
 #include <algorithm>
@@ -42,17 +57,23 @@
 namespace bl {
 namespace {
 
-constexpr int kRows = 16;  // rows per warp tile (two lanes per row)
+constexpr int kRows = 16;     // rows per tile (two lanes per row)
+constexpr int kWarps = 16;    // warps per CTA
+constexpr int kThreads = 32 * kWarps;
+constexpr int kExtraMax = 4;
+constexpr int kResidentSmem = 110 * 1024;  // resident-mode budget: two CTAs fit on an SM  // leftover rows of a CTA taken one at a time (else a partial tile)
 
 struct Geom {
-  int N, K, nC;        // rows, columns, 128-element groups per row
-  int wk, wr;          // warps per row tile (K split), row tiles per CTA
-  int stages;          // ring depth per warp
-  int ntiles;          // ceil(N / kRows)
-  int rowstride;       // bytes per row in a ring buffer (odd multiple of 16)
-  int xbytes;          // bytes of x (K * element size)
+  int N, K, nC;     // rows, columns, 128-element groups per row
+  int grid;         // CTAs
+  int q, rem;       // CTA c takes q rows, plus one when c < rem
+  int resident;     // 1: the CTA's rows are copied whole, one bulk copy per row
+  int S;            // groups per chunk at most (ring mode)
+  int stages;       // ring depth per warp (ring mode)
+  int tiles_max;    // tiles of a CTA at most (resident mode)
+  int rowstride;    // bytes per row in a shared-memory buffer (odd multiple of 16)
   uint32_t stage_bytes;
-  uint32_t off_bar, off_stage, off_part, off_x, off_xraw, smem;
+  uint32_t off_bar, off_stage, off_part, off_x, smem;
   unsigned int* err;
 };
 
@@ -63,274 +84,526 @@ struct Rec {
   static constexpr int kWords = (32 * D + D + 2 + 3) / 4 * 4;  // u32 per record, 16-byte multiple
 };
 
-template <int D, bool XB>
-__device__ __forceinline__ void prepare_x(const void* xv, int nC, uint32_t* xrec, int warp, int nwarps, int lane) {
-  constexpr int RW = Rec<D>::kWords;
-  for (int c = warp; c < nC; c += nwarps) {
-    // lane l holds elements 4l..4l+3 of group c: shift class t = l/8
-    // (elements 32t..32t+31), bytes 4w..4w+3 with w = l%8.  xv is 8-byte
-    // (bf16) or 16-byte (fp32) aligned here.
-    float v[4];
-    const int e0 = c * 128 + 4 * lane;
-    if (XB) {
-      const uint2 u = *reinterpret_cast<const uint2*>(reinterpret_cast<const uint16_t*>(xv) + e0);
-      v[0] = __uint_as_float(u.x << 16);
-      v[1] = __uint_as_float(u.x & 0xFFFF0000u);
-      v[2] = __uint_as_float(u.y << 16);
-      v[3] = __uint_as_float(u.y & 0xFFFF0000u);
+// elements e0..e0+3 of x as fp32 (vec: x is 16-byte aligned)
+template <bool XB>
+__device__ __forceinline__ void load4(const void* x, bool vec, int e0, float (&v)[4]) {
+  if (XB) {
+    const uint16_t* p = reinterpret_cast<const uint16_t*>(x) + e0;
+    uint32_t a, b;
+    if (vec) {
+      const uint2 q = *reinterpret_cast<const uint2*>(p);
+      a = q.x;
+      b = q.y;
     } else {
-      const float4 u = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(xv) + e0);
-      v[0] = u.x; v[1] = u.y; v[2] = u.z; v[3] = u.w;
+      a = uint32_t(p[0]) | (uint32_t(p[1]) << 16);
+      b = uint32_t(p[2]) | (uint32_t(p[3]) << 16);
     }
-    // non-negative floats order like their bit patterns
-    const float m = __uint_as_float(redux_max_u32(
-        __float_as_uint(fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3]))))));
-    const int F = m > 0.f ? (8 * D - 1) - exponent_of(m) : 0;
-    // x * 2^F as two exact power-of-two multiplies (each factor a normal float)
-    const int fa = F / 2, fb = F - fa;
-    const float sA = exp2i(fa), sB = exp2i(fb);
-    int X[4];
-#pragma unroll
-    for (int b = 0; b < 4; ++b) {
-      constexpr int kLim = int((1u << (8 * D - 1)) - 1u);  // keep the top byte signed
-      X[b] = max(-kLim, min(kLim, __float2int_rn(__fmul_rn(__fmul_rn(v[b], sA), sB))));
-    }
-    uint32_t* rec = xrec + c * RW;
-    const int t = lane >> 3, w = lane & 7, sh = 3 - t;
-#pragma unroll
-    for (int d = 0; d < D; ++d) {
-      // byte d of the four values, element b in byte b
-      const uint32_t sel = uint32_t(d) | (uint32_t(d + 4) << 4);
-      const uint32_t lo = __byte_perm(uint32_t(X[0]), uint32_t(X[1]), sel);
-      const uint32_t hi = __byte_perm(uint32_t(X[2]), uint32_t(X[3]), sel);
-      const uint32_t dig = __byte_perm(lo, hi, 0x5410);
-      rec[(w * 4 + sh) * D + d] = dig;
-      const int s = redux_add(d == D - 1 ? dp4a_us(0x01010101u, dig, 0) : dp4a_uu(0x01010101u, dig, 0));
-      if (lane == 0) reinterpret_cast<int*>(rec)[32 * D + d] = s;
-    }
-    if (lane == 0) {
-      reinterpret_cast<float*>(rec)[32 * D + D] = exp2i(-fa);
-      reinterpret_cast<float*>(rec)[32 * D + D + 1] = exp2i(-fb);
+    v[0] = __uint_as_float(a << 16);
+    v[1] = __uint_as_float(a & 0xFFFF0000u);
+    v[2] = __uint_as_float(b << 16);
+    v[3] = __uint_as_float(b & 0xFFFF0000u);
+  } else {
+    const float* p = reinterpret_cast<const float*>(x) + e0;
+    if (vec) {
+      const float4 q = *reinterpret_cast<const float4*>(p);
+      v[0] = q.x; v[1] = q.y; v[2] = q.z; v[3] = q.w;
+    } else {
+      v[0] = p[0]; v[1] = p[1]; v[2] = p[2]; v[3] = p[3];
     }
   }
 }
 
+// One group's record from the 4 elements each lane holds: lane l holds
+// elements 4l..4l+3, i.e. shift class t = l/8 (elements 32t..32t+31) and
+// bytes 4w..4w+3 with w = l%8.  Whole warp.
+template <int D>
+__device__ __forceinline__ void prep_group(const float (&v)[4], uint32_t* rec, int lane) {
+  // non-negative floats order like their bit patterns
+  const float m = __uint_as_float(redux_max_u32(
+      __float_as_uint(fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3]))))));
+  const int F = m > 0.f ? (8 * D - 1) - exponent_of(m) : 0;
+  // x * 2^F as two exact power-of-two multiplies (each factor a normal float)
+  const int fa = F / 2, fb = F - fa;
+  const float sA = exp2i(fa), sB = exp2i(fb);
+  int X[4];
+#pragma unroll
+  for (int b = 0; b < 4; ++b) {
+    constexpr int kLim = int((1u << (8 * D - 1)) - 1u);  // keep the top byte signed
+    X[b] = max(-kLim, min(kLim, __float2int_rn(__fmul_rn(__fmul_rn(v[b], sA), sB))));
+  }
+  const int t = lane >> 3, w = lane & 7, sh = 3 - t;
+#pragma unroll
+  for (int d = 0; d < D; ++d) {
+    // byte d of the four values, element b in byte b
+    const uint32_t sel = uint32_t(d) | (uint32_t(d + 4) << 4);
+    const uint32_t lo = __byte_perm(uint32_t(X[0]), uint32_t(X[1]), sel);
+    const uint32_t hi = __byte_perm(uint32_t(X[2]), uint32_t(X[3]), sel);
+    const uint32_t dig = __byte_perm(lo, hi, 0x5410);
+    rec[(w * 4 + sh) * D + d] = dig;
+    const int s = redux_add(d == D - 1 ? dp4a_us(0x01010101u, dig, 0) : dp4a_uu(0x01010101u, dig, 0));
+    if (lane == 0) reinterpret_cast<int*>(rec)[32 * D + d] = s;
+  }
+  if (lane == 0) {
+    reinterpret_cast<float*>(rec)[32 * D + D] = exp2i(-fa);
+    reinterpret_cast<float*>(rec)[32 * D + D + 1] = exp2i(-fb);
+  }
+}
+
+// Records of all nC groups, warp w taking groups w, w+16, ...; the loads of
+// up to four groups are in flight together.
+template <int D, bool XB>
+__device__ __forceinline__ void prepare_x(const void* x, bool vec, int nC, uint32_t* xrec, int warp, int lane) {
+  constexpr int RW = Rec<D>::kWords;
+  for (int c0 = warp; c0 < nC; c0 += 4 * kWarps) {
+    float v[4][4];
+#pragma unroll
+    for (int b = 0; b < 4; ++b)
+      if (c0 + b * kWarps < nC) load4<XB>(x, vec, (c0 + b * kWarps) * 128 + 4 * lane, v[b]);
+#pragma unroll
+    for (int b = 0; b < 4; ++b)
+      if (c0 + b * kWarps < nC) prep_group<D>(v[b], xrec + (c0 + b * kWarps) * RW, lane);
+  }
+}
+
+// sum_k w_k x_k over one group of two rows: `wa`, `wb` hold the rows' 32
+// packed bytes of the group, `rec` the group's activation record; the
+// results are added to ya, yb.  Each digit word read from shared memory
+// serves both rows.
+template <int D>
+__device__ __forceinline__ void group_dot2(const uint8_t* wa, const uint8_t* wb, const uint32_t* rec, float& ya,
+                                           float& yb) {
+  // [row][digit]: shift classes 0 and 1 (codes), 2 and 3 (16 * codes)
+  int aA[2][D], aB[2][D];
+#pragma unroll
+  for (int i = 0; i < 2; ++i)
+#pragma unroll
+    for (int d = 0; d < D; ++d) aA[i][d] = aB[i][d] = 0;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const uint4 va = *reinterpret_cast<const uint4*>(wa + 16 * h);
+    const uint4 vb = *reinterpret_cast<const uint4*>(wb + 16 * h);
+    const uint32_t wds[2][4] = {{va.x, va.y, va.z, va.w}, {vb.x, vb.y, vb.z, vb.w}};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      // digits of word 4h+j: [4 shifts][D] u32, shared by the lanes on this group
+      uint32_t xw[4 * D];
+#pragma unroll
+      for (int k = 0; k < D; ++k) {
+        const uint4 q = *reinterpret_cast<const uint4*>(rec + ((4 * h + j) * 4) * D + 4 * k);
+        xw[4 * k] = q.x; xw[4 * k + 1] = q.y; xw[4 * k + 2] = q.z; xw[4 * k + 3] = q.w;
+      }
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const uint32_t w = wds[i][j], w2 = w >> 2;
+        const uint32_t m0 = w & 0x03030303u, m1 = w2 & 0x03030303u;
+        const uint32_t m2 = w & 0x30303030u, m3 = w2 & 0x30303030u;
+#pragma unroll
+        for (int d = 0; d < D - 1; ++d) {  // unsigned low bytes
+          aA[i][d] = dp4a_uu(m0, xw[0 * D + d], aA[i][d]);
+          aA[i][d] = dp4a_uu(m1, xw[1 * D + d], aA[i][d]);
+          aB[i][d] = dp4a_uu(m2, xw[2 * D + d], aB[i][d]);
+          aB[i][d] = dp4a_uu(m3, xw[3 * D + d], aB[i][d]);
+        }
+        aA[i][D - 1] = dp4a_us(m0, xw[0 * D + D - 1], aA[i][D - 1]);  // signed top byte
+        aA[i][D - 1] = dp4a_us(m1, xw[1 * D + D - 1], aA[i][D - 1]);
+        aB[i][D - 1] = dp4a_us(m2, xw[2 * D + D - 1], aB[i][D - 1]);
+        aB[i][D - 1] = dp4a_us(m3, xw[3 * D + D - 1], aB[i][D - 1]);
+      }
+    }
+  }
+  const int* sums = reinterpret_cast<const int*>(rec + 32 * D);
+  const float* f = reinterpret_cast<const float*>(rec + 32 * D + D);
+  float p[2];
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    float sc = 1.f;
+    p[i] = 0.f;
+#pragma unroll
+    for (int d = 0; d < D; ++d) {
+      p[i] += float(aA[i][d] + (aB[i][d] >> 4) - sums[d]) * sc;  // aB is a multiple of 16
+      sc *= 256.f;
+    }
+  }
+  ya += (p[0] * f[0]) * f[1];
+  yb += (p[1] * f[0]) * f[1];
+}
+
+template <bool YB>
+__device__ __forceinline__ void store_y(void* y, int row, float v) {
+  if (YB)
+    reinterpret_cast<uint16_t*>(y)[row] = f32_to_bf16_bits_rn(v);
+  else
+    reinterpret_cast<float*>(y)[row] = v;
+}
+
+// Walks a warp's units: first its tile units [a0, a1), then its single-row
+// units [b0, b1), in chunks of at most S groups that never cross a tile or
+// row.  `idx` is the tile (phase 0) or single row (phase 1) of the chunk.
+struct Cursor {
+  int phase, at, end, idx, gg;
+  int b0, b1, nC, S;
+  __device__ __forceinline__ void start(int a0_, int a1_, int b0_, int b1_, int nC_, int S_) {
+    b0 = b0_;
+    b1 = b1_;
+    nC = nC_;
+    S = S_;
+    phase = 0;
+    set(a0_, a1_);
+    if (at >= end) next_phase();
+  }
+  __device__ __forceinline__ void set(int a, int e) {
+    at = a;
+    end = e;
+    idx = a / nC;
+    gg = a - idx * nC;
+  }
+  __device__ __forceinline__ void next_phase() {
+    if (phase == 0) {
+      phase = 1;
+      set(b0, b1);
+      if (at < end) return;
+    }
+    phase = 2;
+  }
+  __device__ __forceinline__ bool done() const { return phase == 2; }
+  __device__ __forceinline__ int len() const { return min(min(S, nC - gg), end - at); }
+  __device__ __forceinline__ void advance(int n) {
+    at += n;
+    gg += n;
+    if (gg == nC) {
+      gg = 0;
+      ++idx;
+    }
+    if (at == end) next_phase();
+  }
+};
+
 template <int D, bool XB, bool YB>
-__global__ void __launch_bounds__(512) gemv_i2s_kernel(const uint8_t* __restrict__ packed, const void* __restrict__ x,
-                                                       void* __restrict__ y, Geom g, int early_weights) {
+__global__ void __launch_bounds__(kThreads) gemv_i2s_kernel(const uint8_t* __restrict__ packed, const void* __restrict__ x,
+                                                            void* __restrict__ y, Geom g, int early_weights) {
   extern __shared__ __align__(128) uint8_t smem[];
   constexpr int RW = Rec<D>::kWords;
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
-  const int nwarps = blockDim.x >> 5;
-  const int rt = warp / g.wk;  // row tile slot of this warp
-  const int ks = warp % g.wk;  // group range of this warp
-  const int c0 = ks * g.nC / g.wk, c1 = (ks + 1) * g.nC / g.wk;
-  const int nchunks = c1 - c0;
-  const int r = lane & (kRows - 1);  // row of the tile
-  const int u = lane >> 4;            // which alternate groups
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + g.off_bar) + warp * g.stages;
-  uint64_t* xbar = reinterpret_cast<uint64_t*>(smem + g.off_bar) + nwarps * g.stages;
-  uint64_t* tbar = xbar + 1 + rt;  // row-tile slot barrier: the wk warps of a tile meet here
-  uint8_t* ring = smem + g.off_stage + size_t(warp) * g.stages * g.stage_bytes;
-  float* part = reinterpret_cast<float*>(smem + g.off_part);
+  const int ir = lane & (kRows - 1);  // row a lane < 16 copies into a ring buffer
+  const int q = lane & 7;              // tile rows q and q+8 of this lane
+  const int u = lane >> 3;             // groups u, u+4, ... of a chunk
+  // ring mode: `stages` buffers per warp; resident mode: the CTA's rows, one
+  // barrier per tile and one for the single rows
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + g.off_bar) + (g.resident ? 0 : warp * g.stages);
+  uint8_t* ring = smem + g.off_stage + (g.resident ? size_t(0) : size_t(warp) * g.stages * g.stage_bytes);
+  float* part_t = reinterpret_cast<float*>(smem + g.off_part);  // [kWarps][2][kRows]
+  float* part_r = part_t + kWarps * 2 * kRows;                   // [kWarps][2]
   uint32_t* xrec = reinterpret_cast<uint32_t*>(smem + g.off_x);
-  uint8_t* xraw = smem + g.off_xraw;
   __shared__ int abort_flag;
+  __shared__ int wspan[kWarps][4];  // first/last tile, first/last single row of each warp (-1: none)
 
-  const int tile_stride = int(gridDim.x) * g.wr;
-  const int first = int(blockIdx.x) * g.wr + rt;
-  const int my_tiles = first < g.ntiles ? (g.ntiles - 1 - first) / tile_stride + 1 : 0;
-  const uint32_t slice_bytes = uint32_t(nchunks) * 32;
+  // rows of this CTA, covered by `ntile` tiles and `nextra` single rows
+  const int c = blockIdx.x;
+  const int r0 = c * g.q + min(c, g.rem);
+  const int rows = g.q + (c < g.rem ? 1 : 0);
+  int ntile = rows / kRows, nextra = rows % kRows;
+  if (nextra > kExtraMax) {
+    ++ntile;
+    nextra = 0;
+  }
+  const int tile_rows = rows - nextra;
+  const int TU = ntile * g.nC, RU = nextra * g.nC;
+  auto split = [&](int n, int w) { return w * (n / kWarps) + min(w, n % kWarps); };
+  const int ta = split(TU, warp), tb = split(TU, warp + 1);
+  const int ra = split(RU, warp), rb = split(RU, warp + 1);
   const int64_t row_bytes = g.K / 4;
 
-  // lanes 0..15 copy their row's group range of local tile i into ring buffer i % stages
-  auto issue = [&](int i) {
-    const int t = first + i * tile_stride;
-    const int s = i % g.stages;
-    const int row = t * kRows + r;
-    const int nrows = min(kRows, g.N - t * kRows);
-    if (lane == 0) mbar_arrive_expect_tx(&full[s], uint32_t(nrows) * slice_bytes);
-    __syncwarp();
-    if (u == 0 && row < g.N)
-      bulk_g2s(ring + size_t(s) * g.stage_bytes + size_t(r) * g.rowstride, packed + int64_t(row) * row_bytes + 32 * c0,
-               slice_bytes, &full[s], policy_evict_first());
+  Cursor ic;  // issue cursor, runs `stages` chunks ahead of the compute cursor (ring mode)
+  ic.start(ta, tb, ra, rb, g.nC, g.S);
+  if (g.resident) ic.phase = 2;
+  int issued = 0;
+  auto issue_next = [&]() {
+    if (ic.done()) return;
+    const int s = issued % g.stages;
+    const int n = ic.len();
+    uint8_t* dst = ring + size_t(s) * g.stage_bytes;
+    if (ic.phase == 0) {
+      const int nrows = min(kRows, tile_rows - ic.idx * kRows);
+      if (lane == 0) mbar_arrive_expect_tx(&full[s], uint32_t(nrows * n * 32));
+      __syncwarp();
+      if (lane < kRows && ir < nrows)
+        bulk_g2s(dst + size_t(ir) * g.rowstride, packed + int64_t(r0 + ic.idx * kRows + ir) * row_bytes + 32 * ic.gg,
+                 uint32_t(n * 32), &full[s], policy_evict_first());
+    } else if (lane == 0) {
+      mbar_arrive_expect_tx(&full[s], uint32_t(n * 32));
+      bulk_g2s(dst, packed + int64_t(r0 + tile_rows + ic.idx) * row_bytes + 32 * ic.gg, uint32_t(n * 32), &full[s],
+               policy_evict_first());
+    }
+    ic.advance(n);
+    ++issued;
   };
 
-  if (lane == 0)
+  if (g.resident) {
+    if (threadIdx.x <= ntile) mbar_init(&full[threadIdx.x], 1);
+  } else if (lane == 0) {
     for (int s = 0; s < g.stages; ++s) mbar_init(&full[s], 1);
-  if (threadIdx.x == 0) {
-    mbar_init(xbar, 1);
-    for (int k = 0; k < g.wr; ++k) mbar_init(xbar + 1 + k, 32 * g.wk);
-    abort_flag = 0;
   }
+  if (lane == 0) {
+    wspan[warp][0] = tb > ta ? ta / g.nC : -1;
+    wspan[warp][1] = tb > ta ? (tb - 1) / g.nC : -1;
+    wspan[warp][2] = rb > ra ? ra / g.nC : -1;
+    wspan[warp][3] = rb > ra ? (rb - 1) / g.nC : -1;
+  }
+  if (threadIdx.x == 0) abort_flag = 0;
   fence_barrier_init();
   __syncthreads();
-  const int npre = min(my_tiles, g.stages);
-  if (early_weights)
-    for (int i = 0; i < npre; ++i) issue(i);
+  // resident mode: one bulk copy per row of the CTA, tile i completing on
+  // barrier i and the single rows on barrier ntile
+  auto issue_rows = [&]() {
+    if (threadIdx.x <= ntile) {
+      const int nr = threadIdx.x < ntile ? min(kRows, tile_rows - int(threadIdx.x) * kRows) : nextra;
+      mbar_arrive_expect_tx(&full[threadIdx.x], uint32_t(nr) * uint32_t(row_bytes));
+    }
+    if (int(threadIdx.x) < rows) {
+      const int t = threadIdx.x;
+      bulk_g2s(ring + size_t(t) * g.rowstride, packed + int64_t(r0 + t) * row_bytes, uint32_t(row_bytes),
+               &full[t < tile_rows ? t / kRows : ntile], policy_evict_first());
+    }
+  };
+  if (early_weights) {
+    if (g.resident)
+      issue_rows();
+    else
+      for (int i = 0; i < g.stages; ++i) issue_next();
+  }
   pdl_wait();
-  // activations: one bulk copy when aligned, else plain loads into the same buffer
-  const bool x_bulk = (reinterpret_cast<uintptr_t>(x) & 15) == 0;
-  if (threadIdx.x == 0 && x_bulk) {
-    mbar_arrive_expect_tx(xbar, uint32_t(g.xbytes));
-    bulk_g2s(xraw, x, uint32_t(g.xbytes), xbar, policy_evict_first());
+  if (!early_weights) {
+    if (g.resident)
+      issue_rows();
+    else
+      for (int i = 0; i < g.stages; ++i) issue_next();
   }
-  if (!early_weights)
-    for (int i = 0; i < npre; ++i) issue(i);
-  if (x_bulk) {
-    if (!mbar_wait_bounded(xbar, 0, g.err)) abort_flag = 1;
-  } else {
-    for (int k = threadIdx.x; k < g.xbytes / 2; k += blockDim.x)
-      reinterpret_cast<uint16_t*>(xraw)[k] = reinterpret_cast<const uint16_t*>(x)[k];
-    __syncthreads();
-  }
-  prepare_x<D, XB>(xraw, g.nC, xrec, warp, nwarps, lane);
+  const bool xvec = (reinterpret_cast<uintptr_t>(x) & 15) == 0;
+  prepare_x<D, XB>(x, xvec, g.nC, xrec, warp, lane);
   const float wscale = *reinterpret_cast<const float*>(packed + int64_t(g.N) * row_bytes);
   __syncthreads();
   pdl_launch_dependents();
 
-  for (int i = 0; i < my_tiles; ++i) {
+  // ---- the warp's units, chunk by chunk -------------------------------------
+  Cursor cc;
+  cc.start(ta, tb, ra, rb, g.nC, g.resident ? g.nC : g.S);
+  float yacc = 0.f, yacc2 = 0.f;  // tile rows q and q+8, or the single row
+  const int lw = lane & 7, lsh = 3 - (lane >> 3);  // single rows: word and shift index of this lane
+  for (int i = 0; !cc.done(); ++i) {
     const int s = i % g.stages;
-    const int t = first + i * tile_stride;
-    if (!abort_flag && !mbar_wait_bounded(&full[s], uint32_t(i / g.stages) & 1u, g.err)) abort_flag = 1;
+    const int n = cc.len();
+    const int phase = cc.phase, idx = cc.idx, gg = cc.gg;
+    const int seg_lo = max(phase == 0 ? ta : ra, idx * g.nC);
+    if (g.resident) {
+      if (!abort_flag && !mbar_wait_bounded(&full[phase == 0 ? idx : ntile], 0, g.err)) abort_flag = 1;
+    } else if (!abort_flag && !mbar_wait_bounded(&full[s], uint32_t(i / g.stages) & 1u, g.err)) {
+      abort_flag = 1;
+    }
     __syncwarp();
-    const uint8_t* myrow = ring + size_t(s) * g.stage_bytes + size_t(r) * g.rowstride;
-    float yacc = 0.f;
-    for (int cc = u; cc < nchunks; cc += 2) {
-      const uint32_t* rec = xrec + (c0 + cc) * RW;
-      // two independent accumulator sets (one per 16-byte half) shorten the dp4a chains
-      int aA[2][D], aB[2][D];
+    // this chunk's bytes: group gg of the first row (+32 per group, + rowstride per row)
+    const uint8_t* buf = g.resident ? ring + size_t(phase == 0 ? idx * kRows : tile_rows + idx) * g.rowstride + 32 * gg
+                                    : ring + size_t(s) * g.stage_bytes;
+    if (phase == 0) {
+      const uint8_t* rowa = buf + size_t(q) * g.rowstride;
+      const uint8_t* rowb = rowa + size_t(8) * g.rowstride;
+      for (int k = u; k < n; k += 4) group_dot2<D>(rowa + 32 * k, rowb + 32 * k, xrec + (gg + k) * RW, yacc, yacc2);
+    } else {
+      for (int k = 0; k < n; ++k) {
+        const uint32_t* rec = xrec + (gg + k) * RW;
+        const uint32_t wd = *reinterpret_cast<const uint32_t*>(buf + 32 * k + 4 * lw);
+        const uint32_t m = (wd >> (2 * lsh)) & 0x03030303u;
+        // sum over this lane's 4 elements of (code - 1) * X, exact per digit;
+        // a zero-weight row gives exactly zero in every lane
+        float p = 0.f, sc = 1.f;
 #pragma unroll
-      for (int h = 0; h < 2; ++h)
-#pragma unroll
-        for (int d = 0; d < D; ++d) aA[h][d] = aB[h][d] = 0;
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const uint4 wv = *reinterpret_cast<const uint4*>(myrow + 32 * cc + 16 * h);
-        const uint32_t wds[4] = {wv.x, wv.y, wv.z, wv.w};
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          // digits of word 4h+j: [4 shifts][D] u32, shared by the lanes on this group
-          uint32_t xw[4 * D];
-#pragma unroll
-          for (int k = 0; k < D; ++k) {
-            const uint4 q = *reinterpret_cast<const uint4*>(rec + ((4 * h + j) * 4) * D + 4 * k);
-            xw[4 * k] = q.x; xw[4 * k + 1] = q.y; xw[4 * k + 2] = q.z; xw[4 * k + 3] = q.w;
+        for (int d = 0; d < D; ++d) {
+          const uint32_t dig = rec[(lw * 4 + lsh) * D + d];
+          const int a = d == D - 1 ? dp4a_us(m, dig, 0) - dp4a_us(0x01010101u, dig, 0)
+                                   : dp4a_uu(m, dig, 0) - dp4a_uu(0x01010101u, dig, 0);
+          p += float(a) * sc;
+          sc *= 256.f;
+        }
+        const float* f = reinterpret_cast<const float*>(rec + 32 * D + D);
+        yacc += (p * f[0]) * f[1];
+      }
+    }
+    __syncwarp();
+    if (!g.resident) issue_next();  // the buffer just read takes chunk i + stages
+    cc.advance(n);
+    const bool seg_end = gg + n == g.nC || cc.phase != phase;
+    if (!seg_end) continue;
+    const bool whole = seg_lo == idx * g.nC && gg + n == g.nC;
+    const int kind = seg_lo == (phase == 0 ? ta : ra) ? 0 : 1;
+    if (phase == 0) {
+      // the four group classes of rows q and q+8: lanes q, q+8, q+16, q+24
+      float va = yacc + __shfl_xor_sync(0xffffffffu, yacc, 8);
+      float vb = yacc2 + __shfl_xor_sync(0xffffffffu, yacc2, 8);
+      va += __shfl_xor_sync(0xffffffffu, va, 16);
+      vb += __shfl_xor_sync(0xffffffffu, vb, 16);
+      const int nrows = min(kRows, tile_rows - idx * kRows);
+      if (u == 0) {
+        if (whole) {
+          if (!abort_flag) {
+            if (q < nrows) store_y<YB>(y, r0 + idx * kRows + q, va * wscale);
+            if (q + 8 < nrows) store_y<YB>(y, r0 + idx * kRows + q + 8, vb * wscale);
           }
-          const uint32_t w = wds[j], w2 = w >> 2;
-          const uint32_t m0 = w & 0x03030303u, m1 = w2 & 0x03030303u;
-          const uint32_t m2 = w & 0x30303030u, m3 = w2 & 0x30303030u;
-#pragma unroll
-          for (int d = 0; d < D - 1; ++d) {  // unsigned low bytes
-            aA[h][d] = dp4a_uu(m0, xw[0 * D + d], aA[h][d]);
-            aA[h][d] = dp4a_uu(m1, xw[1 * D + d], aA[h][d]);
-            aB[h][d] = dp4a_uu(m2, xw[2 * D + d], aB[h][d]);
-            aB[h][d] = dp4a_uu(m3, xw[3 * D + d], aB[h][d]);
-          }
-          aA[h][D - 1] = dp4a_us(m0, xw[0 * D + D - 1], aA[h][D - 1]);  // signed top byte
-          aA[h][D - 1] = dp4a_us(m1, xw[1 * D + D - 1], aA[h][D - 1]);
-          aB[h][D - 1] = dp4a_us(m2, xw[2 * D + D - 1], aB[h][D - 1]);
-          aB[h][D - 1] = dp4a_us(m3, xw[3 * D + D - 1], aB[h][D - 1]);
+        } else {
+          part_t[(warp * 2 + kind) * kRows + q] = va;
+          part_t[(warp * 2 + kind) * kRows + q + 8] = vb;
         }
       }
-      const int* sums = reinterpret_cast<const int*>(rec + 32 * D);
-      float p = 0.f, sc = 1.f;
-#pragma unroll
-      for (int d = 0; d < D; ++d) {
-        p += float(aA[0][d] + aA[1][d] + ((aB[0][d] + aB[1][d]) >> 4) - sums[d]) * sc;
-        sc *= 256.f;
-      }
-      const float* f = reinterpret_cast<const float*>(rec + 32 * D + D);
-      yacc += (p * f[0]) * f[1];
-    }
-    // lanes l and l+16 hold the two halves of row l (same order on both)
-    yacc += __shfl_xor_sync(0xffffffffu, yacc, 16);
-    __syncwarp();
-    if (i + g.stages < my_tiles) issue(i + g.stages);
-    const int row = t * kRows + r;
-    if (g.wk == 1) {
-      if (u == 0 && row < g.N) {
-        const float yv = yacc * wscale;
-        if (YB)
-          reinterpret_cast<uint16_t*>(y)[row] = f32_to_bf16_bits_rn(yv);
-        else
-          reinterpret_cast<float*>(y)[row] = yv;
-      }
     } else {
-      float* pp = part + ((rt * 2 + (i & 1)) * g.wk) * kRows;
-      if (u == 0) pp[ks * kRows + r] = yacc;
-      // all wk warps of the tile arrive and wait, so none can run a tile ahead
-      mbar_arrive(tbar);
-      if (!mbar_wait_bounded(tbar, uint32_t(i) & 1u, g.err)) abort_flag = 1;
-      if (ks == 0 && u == 0 && row < g.N) {
-        float acc = 0.f;
-        for (int k = 0; k < g.wk; ++k) acc += pp[k * kRows + r];
-        const float yv = acc * wscale;
-        if (YB)
-          reinterpret_cast<uint16_t*>(y)[row] = f32_to_bf16_bits_rn(yv);
-        else
-          reinterpret_cast<float*>(y)[row] = yv;
+      const float v = warp_sum(yacc);
+      if (lane == 0) {
+        if (whole) {
+          if (!abort_flag) store_y<YB>(y, r0 + tile_rows + idx, v * wscale);
+        } else {
+          part_r[warp * 2 + kind] = v;
+        }
+      }
+    }
+    yacc = 0.f;
+    yacc2 = 0.f;
+  }
+  __syncthreads();
+
+  // ---- tiles and rows cut between warps: the first warp touching one sums
+  //      the pieces in warp order.  Lane w (< 16) holds warp w's spans; a
+  //      ballot gives the warps touching a tile, and the pieces of all 16
+  //      warps are loaded at once (zero where a warp does not touch it: adding
+  //      +0.0 in order changes no sum) ------------------------------------------
+  int sp[4] = {-1, -1, -1, -1};
+  if (lane < kWarps)
+#pragma unroll
+    for (int k = 0; k < 4; ++k) sp[k] = wspan[lane][k];
+#pragma unroll
+  for (int ph = 0; ph < 2; ++ph) {
+    const int lo = ph == 0 ? ta : ra, hi = ph == 0 ? tb : rb;
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const int t = __shfl_sync(0xffffffffu, sp[2 * ph + k], warp);
+      const int tf = __shfl_sync(0xffffffffu, sp[2 * ph], warp);
+      if (hi <= lo || (k == 1 && t == tf)) continue;  // nothing, or one tile/row: stored as the first segment
+      const int t0 = t * g.nC;
+      if (lo <= t0 && t0 + g.nC <= hi) continue;  // whole inside this warp: already written
+      const unsigned int touch = __ballot_sync(0xffffffffu, sp[2 * ph] >= 0 && sp[2 * ph] <= t && t <= sp[2 * ph + 1]);
+      if ((__ffs(touch) - 1) != warp) continue;  // an earlier warp owns it
+      float acc = 0.f;
+      if (ph == 0) {
+        if (lane < kRows) {
+          float v[kWarps];
+#pragma unroll
+          for (int w2 = 0; w2 < kWarps; ++w2)
+            v[w2] = (touch >> w2) & 1u ? part_t[(w2 * 2 + (w2 == warp ? k : 0)) * kRows + lane] : 0.f;
+#pragma unroll
+          for (int w2 = 0; w2 < kWarps; ++w2) acc += v[w2];
+        }
+        const int nrows = min(kRows, tile_rows - t * kRows);
+        if (lane < nrows && !abort_flag) store_y<YB>(y, r0 + t * kRows + lane, acc * wscale);
+      } else if (lane == 0) {
+        float v[kWarps];
+#pragma unroll
+        for (int w2 = 0; w2 < kWarps; ++w2) v[w2] = (touch >> w2) & 1u ? part_r[w2 * 2 + (w2 == warp ? k : 0)] : 0.f;
+#pragma unroll
+        for (int w2 = 0; w2 < kWarps; ++w2) acc += v[w2];
+        if (!abort_flag) store_y<YB>(y, r0 + tile_rows + t, acc * wscale);
       }
     }
   }
+
   if (abort_flag && lane == 0) {
     // let copies still in flight land (bounded) before the CTA exits
-    for (int j = 0; j < my_tiles && j < g.stages; ++j) mbar_wait_bounded(&full[j], 0, nullptr);
-    if (warp == 0) mbar_wait_bounded(xbar, 0, nullptr);
+    if (g.resident) {
+      if (warp == 0)
+        for (int j = 0; j <= ntile; ++j) mbar_wait_bounded(&full[j], 0, nullptr);
+    } else {
+      for (int j = 0; j < g.stages && j < issued; ++j) mbar_wait_bounded(&full[j], 0, nullptr);
+    }
   }
 }
 
 template <int D>
-bool plan(Geom& g, int64_t N, int64_t K, int esize, int max_smem, int nsm) {
+bool plan(Geom& g, int64_t N, int64_t K, int max_smem, int nsm) {
   auto up = [](uint64_t v, uint64_t a) { return (v + a - 1) / a * a; };
   g.N = int(N);
   g.K = int(K);
   g.nC = int(K / 128);
-  g.xbytes = int(K * esize);
-  g.ntiles = int((N + kRows - 1) / kRows);
-  // Split the groups of a tile over up to 16 warps while every warp keeps
-  // at least two groups and there are fewer than ~16 warps per SM; then put
-  // as many row tiles in a CTA as keep it at <= 16 warps without dropping
-  // below one CTA per SM.  More warps per CTA also spread the per-CTA
-  // activation preparation thinner.
-  int wk = 1;
-  while (wk < 16 && int64_t(g.ntiles) * wk < 16LL * nsm && g.nC / (wk + 1) >= 2) ++wk;
-  g.wk = wk;
-  int wr = std::max(1, 16 / wk);
-  while (wr > 1 && (g.ntiles + wr - 1) / wr < nsm) --wr;
-  g.wr = wr;
-  const int max_chunks = (g.nC + wk - 1) / wk;
-  int rs = int(up(uint64_t(max_chunks) * 32, 16));
-  if (((rs / 16) & 1) == 0) rs += 16;
-  g.rowstride = rs;
-  g.stage_bytes = uint32_t(up(uint64_t(kRows) * rs, 128));
-  const int warps = g.wk * g.wr;
-  const int64_t tiles_per_warp = (g.ntiles + int64_t(g.wr) * nsm - 1) / (int64_t(g.wr) * nsm);
-  for (int st = int(std::min<int64_t>(3, std::max<int64_t>(1, tiles_per_warp))); st >= 1; --st) {
+  g.grid = int(std::min<int64_t>(nsm, N));
+  g.q = g.N / g.grid;
+  g.rem = g.N % g.grid;
+  // units per warp at most: the tiles of q+1 rows, or a partial tile
+  const int rows = g.q + (g.rem ? 1 : 0);
+  const int tiles = (rows + kRows - 1) / kRows;
+  const long long per_warp = ((long long)tiles * g.nC + kWarps - 1) / kWarps + (long long)kExtraMax * g.nC / kWarps + 1;
+  const uint64_t fixed_x = up(4ull * g.nC * Rec<D>::kWords, 128);
+  {
+    // resident mode when the CTA's rows fit next to the activation records,
+    // leaving room for a second CTA (the next kernel's) on the SM
+    int rs = int(up(uint64_t(K / 4), 16));
+    if (((rs / 16) & 1) == 0) rs += 16;
+    const int tiles_max = tiles;
+    const uint64_t rows_alloc = uint64_t(tiles_max) * kRows + kExtraMax;
     uint64_t off = 0;
-    g.off_bar = uint32_t(off);
-    off = up(off + 8ull * (warps * st + 1 + g.wr), 128);
-    g.off_stage = uint32_t(off);
-    off = up(off + uint64_t(warps) * st * g.stage_bytes, 128);
-    g.off_part = uint32_t(off);
-    off = up(off + (g.wk > 1 ? 4ull * g.wr * 2 * g.wk * kRows : 0), 128);
-    g.off_x = uint32_t(off);
-    off = up(off + 4ull * g.nC * Rec<D>::kWords, 128);
-    g.off_xraw = uint32_t(off);
-    off = up(off + uint64_t(g.xbytes), 128);
-    if (off <= uint64_t(max_smem)) {
-      g.stages = st;
+    const uint32_t off_bar = uint32_t(off);
+    off = up(off + 8ull * (tiles_max + 1), 128);
+    const uint32_t off_stage = uint32_t(off);
+    off = up(off + rows_alloc * rs, 128);
+    const uint32_t off_part = uint32_t(off);
+    off = up(off + 4ull * kWarps * 2 * (kRows + 1), 128);
+    const uint32_t off_x = uint32_t(off);
+    off += fixed_x;
+    if (off <= uint64_t(std::min(max_smem, kResidentSmem)) && tiles_max + 1 <= kThreads) {
+      g.resident = 1;
+      g.S = g.nC;
+      g.stages = 1;
+      g.tiles_max = tiles_max;
+      g.rowstride = rs;
+      g.stage_bytes = 0;
+      g.off_bar = off_bar;
+      g.off_stage = off_stage;
+      g.off_part = off_part;
+      g.off_x = off_x;
       g.smem = uint32_t(off);
       return true;
     }
+  }
+  g.resident = 0;
+  for (int S = int(std::min<long long>(8, std::max<long long>(1, per_warp))); S >= 1; S = S > 1 ? S / 2 : 0) {
+    int rs = int(up(uint64_t(S) * 32, 16));
+    if (((rs / 16) & 1) == 0) rs += 16;
+    const uint32_t stage_bytes = uint32_t(up(uint64_t(kRows) * rs, 128));
+    const long long chunks = (per_warp + S - 1) / S + 2;  // tile and phase boundaries add a few
+    for (int st = int(std::min<long long>(3, std::max<long long>(1, chunks))); st >= 1; --st) {
+      uint64_t off = 0;
+      const uint32_t off_bar = uint32_t(off);
+      off = up(off + 8ull * kWarps * st, 128);
+      const uint32_t off_stage = uint32_t(off);
+      off = up(off + uint64_t(kWarps) * st * stage_bytes, 128);
+      const uint32_t off_part = uint32_t(off);
+      off = up(off + 4ull * kWarps * 2 * (kRows + 1), 128);
+      const uint32_t off_x = uint32_t(off);
+      off += fixed_x;
+      if (off <= uint64_t(max_smem)) {
+        g.S = S;
+        g.rowstride = rs;
+        g.stage_bytes = stage_bytes;
+        g.stages = st;
+        g.off_bar = off_bar;
+        g.off_stage = off_stage;
+        g.off_part = off_part;
+        g.off_x = off_x;
+        g.smem = uint32_t(off);
+        return true;
+      }
+    }
+    if (S == 1) break;
   }
   return false;
 }
 
 struct Plan {
   Geom g;
-  int grid, threads;
   bool ok;
 };
 
@@ -344,23 +617,16 @@ cudaError_t run(const uint8_t* packed, const void* x, void* y, int64_t N, int64_
   if (!cache.get(dev, N, K, &p)) {
     int max_optin = 0;
     cudaDeviceGetAttribute(&max_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-    const int nsm = sm_count();
-    p.ok = plan<D>(p.g, N, K, XB ? 2 : 4, max_optin - 1024, nsm);
+    p.ok = plan<D>(p.g, N, K, max_optin - 1024, sm_count());
     if (!p.ok) return cudaErrorInvalidConfiguration;
     // the cap is a property of the kernel, shared by every shape: raise it to the maximum once
     cudaError_t e = raise_smem_cap(kern, dev, max_optin - 1024);
     if (e != cudaSuccess) return e;
-    p.threads = 32 * p.g.wk * p.g.wr;
-    int blocks_per_sm = 0;
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks_per_sm, kern, p.threads, p.g.smem);
-    if (blocks_per_sm < 1) blocks_per_sm = 1;
-    p.grid = (p.g.ntiles + p.g.wr - 1) / p.g.wr;
-    if (p.grid > nsm * blocks_per_sm) p.grid = nsm * blocks_per_sm;
     p.g.err = dev_error_ptr();
     cache.put(dev, N, K, p);
   }
   const bool pdl = overlap_enabled();
-  return launch(kern, dim3(p.grid), dim3(p.threads), p.g.smem, st, pdl, packed, x, y, p.g, pdl ? 1 : 0);
+  return launch(kern, dim3(p.g.grid), dim3(kThreads), p.g.smem, st, pdl, packed, x, y, p.g, pdl ? 1 : 0);
 }
 
 }  // namespace
@@ -368,7 +634,7 @@ cudaError_t run(const uint8_t* packed, const void* x, void* y, int64_t N, int64_
 cudaError_t launch_gemv_i2s(const uint8_t* packed, const void* x, bl_dtype xt, void* y, bl_dtype yt, int64_t N,
                             int64_t K, cudaStream_t s) {
   const bool xb = xt == BL_BF16, yb = yt == BL_BF16;
-  if (xb) return yb ? run<3, true, true>(packed, x, y, N, K, s) : run<3, true, false>(packed, x, y, N, K, s);
+  if (xb) return yb ? run<2, true, true>(packed, x, y, N, K, s) : run<3, true, false>(packed, x, y, N, K, s);
   return yb ? run<4, false, true>(packed, x, y, N, K, s) : run<4, false, false>(packed, x, y, N, K, s);
 }
 

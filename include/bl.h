@@ -162,11 +162,12 @@ bl_status bl_quantize_act_absmax_int8(const void* x, bl_dtype xt, int64_t M, int
  *   x      : [K] fp32 (xt = BL_F32) or bf16 (xt = BL_BF16).
  *   y      : [N] fp32 or bf16 (yt).  bf16 output is rounded to nearest even.
  * Accuracy: within each 128-element group x is carried as a fixed-point
- * integer of 30 bits (fp32 input) or 22 bits (bf16 input) relative to the
- * group's max|x|: bf16 inputs within 14 binades of the group maximum and
- * fp32 inputs within 6 binades are carried exactly, smaller values with an
- * absolute error of at most 2^-31 (fp32) / 2^-23 (bf16) times the group
- * maximum.  Products and sums inside a group are exact integers; each group
+ * integer of 30 bits (fp32 input), 22 bits (bf16 input, fp32 output) or 14
+ * bits (bf16 input and output) relative to the group's max|x|: values
+ * within 6, 14 or 6 binades of the group maximum (respectively) are carried
+ * exactly, smaller values with an absolute error of at most 2^-31, 2^-23 or
+ * 2^-15 times the group maximum (the last far below the 2^-9 relative
+ * rounding of a bf16 output).  Products and sums inside a group are exact integers; each group
  * sum is converted to fp32 once and the group sums are added in fp32, then
  * rounded to bf16 if asked.  For activations without extreme in-group
  * outliers the error is within 1e-5 (fp32 output) / 2e-2 (bf16 output) of

@@ -125,6 +125,35 @@ def test_gemv_i2s_small(B, xd, yd, N, K):
     assert_close(y, ref, cond, TOL_F32 if yd == "f32" else TOL_BF16, "gemv_i2s %dx%d %s->%s" % (N, K, xd, yd))
 
 
+@pytest.mark.parametrize("xd,yd", [("f32", "f32"), ("bf16", "bf16")])
+@pytest.mark.parametrize("N", [1, 20, 300])
+def test_gemv_i2s_max_k(B, xd, yd, N):
+    """K = 32768, the largest K bl_gemv_i2s accepts: a single 16-row tile is
+    then split over many CTAs and finished through the stream workspace."""
+    K = 32768
+    g = rng(N + 7)
+    w = ternary(g, N, K)
+    x = rand_x(g, K, xd)
+    y, ref, cond = run_gemv_i2s(B, w, np.float32(0.75), x, xd, yd)
+    assert_close(y, ref, cond, TOL_F32 if yd == "f32" else TOL_BF16, "gemv_i2s %dx%d" % (N, K))
+
+
+def test_gemv_i2s_unaligned_x(B):
+    """x at an element-aligned but not 16-byte-aligned address (plain loads)."""
+    N, K = 70, 1024
+    g = rng(99)
+    w = ternary(g, N, K)
+    for xd in ("f32", "bf16"):
+        x = rand_x(g, K, xd)
+        xg = x_gpu(x, xd)
+        buf = torch.empty(K + 1, dtype=xg.dtype, device="cuda")
+        buf[1:].copy_(xg)
+        packed = B.bl_pack_i2s(to_gpu(w), np.float32(1.0))
+        yv = B.bl_gemv_i2s(packed, buf[1:], N, K, y_dtype=torch.float32).cpu().numpy().astype(np.float64)
+        ref, cond = O.gemv_i2s(O.pack_i2s(w, np.float32(1.0)), x_f64(x, xd), N, K)
+        assert_close(yv, ref, cond, TOL_F32, "gemv_i2s unaligned x " + xd)
+
+
 def test_gemv_i2s_extreme_inputs(B):
     """Degenerate activations: all zero, a 1e4 outlier in one group, tiny
     values (1e-30), all equal; and an all-zero weight row."""
