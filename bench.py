@@ -1,9 +1,10 @@
 """Benchmark of the packed BitLinear hot path on GB300.
 
 Headline workload (one step = the BitNet-2B-shaped MLP for one token):
-    gate  y_g = W_g x   (i2_s, 2560 -> 6912, bf16 in, bf16 out)
-    up    y_u = W_u x   (i2_s, 2560 -> 6912)
-    down  y_d = W_d x_d (i2_s, 6912 -> 2560, x_d a second bf16 vector)
+    h = max(0, W_g x)^2 * (W_u x)   (fused gate/up, i2_s 2560 -> 6912 twice,
+                                     bf16 in, bf16 out; one launch)
+    y = W_d h                       (i2_s 6912 -> 2560, bf16 in/out)
+so the down projection consumes the fused kernel's output, as in the model.
 The three matrices are held in 24 rotating copies (320 MB, more than twice
 the 129 MB L2), so every step streams its weights from HBM.  Steps are
 captured in CUDA graphs (with programmatic dependent launch between the
@@ -12,7 +13,8 @@ a barrier and a device synchronize, timed with CUDA events on the launching
 stream.
 
 metric: packed-weight GB/s = (packed i2_s bytes of the three matrices,
-scales included) * steps / time.  Secondary lines report the other
+scales included) * steps / time.  The roofline object times the dominant
+kernel (the fused gate/up launch) in its own graph of back-to-back launches.  Secondary lines report the other
 workloads (i2_s fp32 2560x2560, TQ2_0 5120x13824, W1A8 LM head at M=1/4/8,
 i2_s int8 prefill at M=512 in TOPS).
 
@@ -62,13 +64,10 @@ def mlp_bytes():
     return sum(packed_bytes(*WL.extra[m]) for m in MATS)
 
 
-def mlp_algorithmic_bytes_per_launch():
-    """Per GEMV launch: packed weights + scale + x (bf16) + y (bf16), averaged over the three."""
-    tot = 0
-    for m in MATS:
-        N, K = WL.extra[m]
-        tot += packed_bytes(N, K) + 2 * K + 2 * N
-    return tot / 3.0
+def gate_up_algorithmic_bytes():
+    """Per fused gate/up launch: both packed tensors (scales included) + x (bf16) + h (bf16)."""
+    N, K = WL.extra["gate"]
+    return 2 * packed_bytes(N, K) + 2 * K + 2 * N
 
 
 # ---------------------------------------------------------------------------
@@ -250,19 +249,15 @@ def bench_ours(args, dist):
             mats[m] = upload_i2s(B, torch, WL.index, "w_" + m, N, K, WL.p_zero,
                                  synth.tensor_scale(WL.index, "scale_" + m), COPIES)
         x_bits = synth.activations(WL.index, 1, 2560, "bf16")[0]
-        xd_bits = synth.activations(WL.index, 1, 6912, "bf16", tensor="x_down")[0]
         x = torch.from_numpy(x_bits.view(np.int16)).cuda().view(torch.bfloat16)
-        xd = torch.from_numpy(xd_bits.view(np.int16)).cuda().view(torch.bfloat16)
-        yg = torch.empty(6912, dtype=torch.bfloat16, device="cuda")
-        yu = torch.empty(6912, dtype=torch.bfloat16, device="cuda")
+        yg = torch.empty(6912, dtype=torch.bfloat16, device="cuda")   # h, the down projection's input
         ydn = torch.empty(2560, dtype=torch.bfloat16, device="cuda")
     torch.cuda.synchronize()
 
     def mlp_step(i):
         c = i % COPIES
-        B.bl_gemv_i2s(mats["gate"][c], x, 6912, 2560, y=yg)
-        B.bl_gemv_i2s(mats["up"][c], x, 6912, 2560, y=yu)
-        B.bl_gemv_i2s(mats["down"][c], xd, 2560, 6912, y=ydn)
+        B.bl_gemv_i2s_gate_up(mats["gate"][c], mats["up"][c], x, 6912, 2560, h=yg)
+        B.bl_gemv_i2s(mats["down"][c], yg, 2560, 6912, y=ydn)
 
     gs = args.graph_steps
     with ClockSampler(torch.cuda.current_device()) as clk:
@@ -270,29 +265,29 @@ def bench_ours(args, dist):
     ms = dist.max(ms)
     step_bytes = mlp_bytes()
     value = step_bytes * args.steps * dist.world / (ms * 1e-3) / 1e9
-    launches = 3 * args.steps
-    avg_launch_s = ms * 1e-3 / launches
-    achieved = mlp_algorithmic_bytes_per_launch() / avg_launch_s / 1e9
+    launches = 2 * args.steps
+
+    # the dominant kernel alone: back-to-back fused gate/up launches (same copies, same PDL setting)
+    def gate_up_only(i):
+        c = i % COPIES
+        B.bl_gemv_i2s_gate_up(mats["gate"][c], mats["up"][c], x, 6912, 2560, h=yg)
+
+    gu_steps = max(gs, (min(args.steps, 20000) // gs) * gs)
+    gu_ms = dist.max(time_graph(torch, dist, gate_up_only, gu_steps, gs, gs, stream))
+    avg_launch_s = gu_ms * 1e-3 / gu_steps
+    achieved = gate_up_algorithmic_bytes() / avg_launch_s / 1e9
 
     # ---- e2e: host buffers, copies inside the timed region, public API per step -------
     e2e_steps = min(args.steps, args.e2e_steps)
     hx = torch.from_numpy(x_bits.view(np.int16).copy()).pin_memory()
-    hxd = torch.from_numpy(xd_bits.view(np.int16).copy()).pin_memory()
-    hyg = torch.empty(6912, dtype=torch.int16).pin_memory()
-    hyu = torch.empty(6912, dtype=torch.int16).pin_memory()
     hyd = torch.empty(2560, dtype=torch.int16).pin_memory()
     dx = torch.empty(2560, dtype=torch.int16, device="cuda")
-    dxd = torch.empty(6912, dtype=torch.int16, device="cuda")
 
     def e2e_step(i):
         c = i % COPIES
         dx.copy_(hx, non_blocking=True)
-        dxd.copy_(hxd, non_blocking=True)
-        B.bl_gemv_i2s(mats["gate"][c], dx.view(torch.bfloat16), 6912, 2560, y=yg)
-        B.bl_gemv_i2s(mats["up"][c], dx.view(torch.bfloat16), 6912, 2560, y=yu)
-        B.bl_gemv_i2s(mats["down"][c], dxd.view(torch.bfloat16), 2560, 6912, y=ydn)
-        hyg.copy_(yg.view(torch.int16), non_blocking=True)
-        hyu.copy_(yu.view(torch.int16), non_blocking=True)
+        B.bl_gemv_i2s_gate_up(mats["gate"][c], mats["up"][c], dx.view(torch.bfloat16), 6912, 2560, h=yg)
+        B.bl_gemv_i2s(mats["down"][c], yg, 2560, 6912, y=ydn)
         hyd.copy_(ydn.view(torch.int16), non_blocking=True)
 
     B.set_overlap(False)
@@ -310,8 +305,8 @@ def bench_ours(args, dist):
         dist.barrier()
     e2e_ms = dist.max(e0.elapsed_time(e1))
     e2e_value = step_bytes * e2e_steps * dist.world / (e2e_ms * 1e-3) / 1e9
-    h2d = 2 * (2560 + 6912)
-    d2h = 2 * (6912 + 6912 + 2560)
+    h2d = 2 * 2560
+    d2h = 2 * 2560
     B.set_overlap(True)
 
     extra = {}
@@ -328,16 +323,19 @@ def bench_ours(args, dist):
         line = {
             "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": dist.world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "int8xint8->int32 (dp4a), fp32 epilogue", "data": "synthetic",
+            "vs_baseline": None, "dtype": "int32",
+            "arith": "dp4a int32 dots of per-group 16-bit fixed-point activation digits and ternary codes; fp32 epilogue", "data": "synthetic",
             "config": {"workload": WL.name, "model": "BitNet-2B-shaped MLP (random ternary weights)",
                        "global_batch": 1, "seq_len": 1, "parallelism": "replicas" if dist.world > 1 else "single",
                        "M": 1, "shapes_NxK": [list(WL.extra[m]) for m in MATS], "x": "bf16", "y": "bf16",
+                       "step": "h = relu(W_gate x)^2 * (W_up x) [one fused launch]; y = W_down h",
                        "weight_copies": COPIES, "l2": "inputs larger than L2 (24 rotating weight copies, 320 MB)",
                        "launch": "CUDA graph of %d steps, programmatic dependent launch" % gs},
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
                          "frac": round(achieved / hbm, 4), "traffic": profiled_traffic(),
-                         "kernel": "gemv_i2s_kernel<3, bf16 x, bf16 y>",
-                         "algorithmic_bytes_per_launch": mlp_algorithmic_bytes_per_launch(),
+                         "kernel": "gemv_i2s_kernel<D=2, bf16 x, bf16 y, gate+up>",
+                         "algorithmic_bytes_per_launch": gate_up_algorithmic_bytes(),
+                         "avg_launch_us": round(avg_launch_s * 1e6, 3),
                          "peak_source": peak_src + " copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"},
             "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "steps": e2e_steps, "api": "gemm_bl_gemv_gb300.binding.bl_gemv_i2s per call, eager"},
@@ -427,7 +425,9 @@ def bench_secondary(args, B, torch, stream, dist, hbm, bf16_peak):
 # ---------------------------------------------------------------------------
 
 class OracleMLP:
-    """The oracle computing the MLP step on `rows_frac` of each matrix's rows."""
+    """The oracle computing the MLP step (fused gate/up, then down) on
+    `rows_frac` of each matrix's rows; the down projection reads the full h of
+    one oracle step computed at construction."""
 
     def __init__(self, rows_frac=1.0):
         from oracle import oracle as O
@@ -442,15 +442,16 @@ class OracleMLP:
             rows = np.linspace(0, N - 1, nr).astype(np.int64)
             self.mats[m] = (O.pack_i2s(w, synth.tensor_scale(WL.index, "scale_" + m)), N, K, rows)
         xb = synth.activations(WL.index, 1, 2560, "bf16")[0]
-        xdb = synth.activations(WL.index, 1, 6912, "bf16", tensor="x_down")[0]
         self.x = O.bf16_to_f64(xb)
-        self.xd = O.bf16_to_f64(xdb)
+        pg, N, K, _ = self.mats["gate"]
+        self.h, _ = O.gemv_i2s_gate_up(pg, self.mats["up"][0], self.x, N, K)
         self.bytes_per_step = sum(len(r) * (K // 4) for (_, _, K, r) in self.mats.values())
 
     def step(self):
-        for m in MATS:
-            p, N, K, rows = self.mats[m]
-            self.O.gemv_i2s(p, self.x if m != "down" else self.xd, N, K, rows=rows)
+        pg, N, K, rows = self.mats["gate"]
+        self.O.gemv_i2s_gate_up(pg, self.mats["up"][0], self.x, N, K, rows=rows)
+        pd, Nd, Kd, rows_d = self.mats["down"]
+        self.O.gemv_i2s(pd, self.h, Nd, Kd, rows=rows_d)
 
 
 def cpu_baseline(seconds):
@@ -464,7 +465,7 @@ def cpu_baseline(seconds):
     dt = time.perf_counter() - t0
     return {"value": round(o.bytes_per_step * n / dt / 1e9, 4), "unit": UNIT, "cores": o.cores if o.O.has_openmp() else 1,
             "kind": "oracle",
-            "sample": "%d full MLP steps (gate+up+down, all rows, one token) in %.1f s" % (n, dt)}
+            "sample": "%d full MLP steps (fused gate/up then down, all rows, one token) in %.1f s" % (n, dt)}
 
 
 def bench_reference(args, dist):

@@ -21,7 +21,7 @@ BL_DEVERR_WAIT_TIMEOUT = 0x1
 EXPORTS = [
     "bl_status_string", "bl_last_error", "bl_device_error", "bl_set_overlap", "bl_get_overlap",
     "bl_pack_i2s", "bl_pack_tq2_0", "bl_pack_w1", "bl_quantize_act_absmax_int8",
-    "bl_gemv_i2s", "bl_gemv_tq2_0", "bl_gemm_w1a8", "bl_gemm_i2s_int8",
+    "bl_gemv_i2s", "bl_gemv_i2s_gate_up", "bl_gemv_tq2_0", "bl_gemm_w1a8", "bl_gemm_i2s_int8",
 ]
 
 
@@ -44,6 +44,7 @@ def _declare(L):
         "bl_pack_w1": ([p, i64, i64, p, p], st),
         "bl_quantize_act_absmax_int8": ([p, i32, i64, i64, p, p, p], st),
         "bl_gemv_i2s": ([p, p, i32, p, i32, i64, i64, p], st),
+        "bl_gemv_i2s_gate_up": ([p, p, p, i32, p, i32, i64, i64, p], st),
         "bl_gemv_tq2_0": ([p, p, i32, p, i64, i64, p], st),
         "bl_gemm_w1a8": ([p, p, p, p, p, i64, i64, i64, i32, p, p, p], st),
         "bl_gemm_i2s_int8": ([p, p, p, i64, i64, i64, p, p, p], st),
@@ -178,6 +179,18 @@ def bl_gemv_i2s(packed, x, N, K, y=None, y_dtype=None, stream=None):
     _check(_lib.bl_gemv_i2s(_ptr(packed), _ptr(x), _dtype_code(x), _ptr(_cuda(y, "y")), _dtype_code(y), N, K,
                             _stream(stream)))
     return y
+
+
+def bl_gemv_i2s_gate_up(packed_gate, packed_up, x, N, K, h=None, h_dtype=None, stream=None):
+    """h = max(0, scale_g * W_g x)^2 * (scale_u * W_u x), one token."""
+    _cuda(packed_gate, "packed_gate")
+    _cuda(packed_up, "packed_up")
+    _cuda(x, "x")
+    if h is None:
+        h = torch.empty(N, dtype=h_dtype or x.dtype, device=x.device)
+    _check(_lib.bl_gemv_i2s_gate_up(_ptr(packed_gate), _ptr(packed_up), _ptr(x), _dtype_code(x), _ptr(_cuda(h, "h")),
+                                    _dtype_code(h), N, K, _stream(stream)))
+    return h
 
 
 def bl_gemv_tq2_0(packed, x, N, K, y=None, stream=None):

@@ -172,6 +172,23 @@ bl_status bl_gemv_i2s(const uint8_t* packed, const void* x, bl_dtype xt, void* y
   return cuda_status(launch_gemv_i2s(packed, x, xt, y, yt, N, K, S(stream)), "bl_gemv_i2s");
 }
 
+bl_status bl_gemv_i2s_gate_up(const uint8_t* packed_gate, const uint8_t* packed_up, const void* x, bl_dtype xt,
+                              void* h, bl_dtype ht, int64_t N, int64_t K, bl_stream_t stream) {
+  if (!packed_gate || !packed_up || !x || !h) return fail(BL_ERR_NULL, "bl_gemv_i2s_gate_up: NULL pointer");
+  if ((xt != BL_F32 && xt != BL_BF16) || (ht != BL_F32 && ht != BL_BF16))
+    return fail(BL_ERR_DTYPE, "bl_gemv_i2s_gate_up: bad dtype (x %d, h %d)", int(xt), int(ht));
+  if (N < 1 || K < 128 || K % 128 || N > 0x7fffffff)
+    return fail(BL_ERR_SHAPE, "bl_gemv_i2s_gate_up: need N >= 1, K %% 128 == 0 (N=%lld K=%lld)", (long long)N,
+                (long long)K);
+  if (K > 32768) return fail(BL_ERR_UNSUPPORTED, "bl_gemv_i2s_gate_up: K up to 32768 supported (K=%lld)", (long long)K);
+  if (!aligned(packed_gate, 16) || !aligned(packed_up, 16))
+    return fail(BL_ERR_ALIGN, "bl_gemv_i2s_gate_up: packed tensors must be 16-byte aligned");
+  if (!aligned(x, xt == BL_F32 ? 4 : 2) || !aligned(h, ht == BL_F32 ? 4 : 2))
+    return fail(BL_ERR_ALIGN, "bl_gemv_i2s_gate_up: x and h must be aligned to their element size");
+  return cuda_status(launch_gemv_i2s_gate_up(packed_gate, packed_up, x, xt, h, ht, N, K, S(stream)),
+                     "bl_gemv_i2s_gate_up");
+}
+
 bl_status bl_gemv_tq2_0(const uint8_t* packed, const void* x, bl_dtype xt, float* y, int64_t N, int64_t K,
                         bl_stream_t stream) {
   if (!packed || !x || !y) return fail(BL_ERR_NULL, "bl_gemv_tq2_0: NULL pointer");

@@ -70,10 +70,11 @@ struct Geom {
   int resident;     // 1: the CTA's rows are copied whole, one bulk copy per row
   int S;            // groups per chunk at most (ring mode)
   int stages;       // ring depth per warp (ring mode)
-  int tiles_max;    // tiles of a CTA at most (resident mode)
+  int tiles_max;    // tiles of a CTA at most
+  int rows_alloc;   // rows of one matrix's resident block (tiles_max * 16 + kExtraMax)
   int rowstride;    // bytes per row in a shared-memory buffer (odd multiple of 16)
   uint32_t stage_bytes;
-  uint32_t off_bar, off_stage, off_part, off_x, smem;
+  uint32_t off_bar, off_stage, off_part, off_res, off_x, smem;
   unsigned int* err;
 };
 
@@ -278,9 +279,16 @@ struct Cursor {
   }
 };
 
-template <int D, bool XB, bool YB>
-__global__ void __launch_bounds__(kThreads) gemv_i2s_kernel(const uint8_t* __restrict__ packed, const void* __restrict__ x,
-                                                            void* __restrict__ y, Geom g, int early_weights) {
+// NM = 1: y = scale * W x.  NM = 2: the fused gate/up product of the MLP,
+// y = max(0, g)^2 * u with g = scale_g * W_g x and u = scale_u * W_u x
+// ("Hesper/Layers/BitLinear", "Fused Gate+Up+ReLU²×Mul M=1 Kernel"): both
+// matrices' rows of the CTA's range are units of the same CTA, and the
+// epilogue runs once both results of a row are final.
+template <int D, bool XB, bool YB, int NM>
+__global__ void __launch_bounds__(kThreads, 2) gemv_i2s_kernel(const uint8_t* __restrict__ packed,
+                                                            const uint8_t* __restrict__ packed2,
+                                                            const void* __restrict__ x, void* __restrict__ y, Geom g,
+                                                            int early_weights) {
   extern __shared__ __align__(128) uint8_t smem[];
   constexpr int RW = Rec<D>::kWords;
   const int lane = threadIdx.x & 31;
@@ -308,7 +316,16 @@ __global__ void __launch_bounds__(kThreads) gemv_i2s_kernel(const uint8_t* __res
     nextra = 0;
   }
   const int tile_rows = rows - nextra;
-  const int TU = ntile * g.nC, RU = nextra * g.nC;
+  // units run over NM matrices: virtual tile v is tile v % ntile of matrix
+  // v / ntile, virtual single row likewise
+  const int TU = NM * ntile * g.nC, RU = NM * nextra * g.nC;
+  auto pk = [&](int m) { return (NM == 2 && m) ? packed2 : packed; };
+  auto vsplit = [&](int v, int per, int& m) {
+    m = (NM == 2 && v >= per) ? 1 : 0;
+    return v - m * per;
+  };
+  const int nbar = ntile + 1;                           // resident barriers per matrix
+  const size_t mat_bytes = size_t(g.rows_alloc) * g.rowstride;  // resident block per matrix
   auto split = [&](int n, int w) { return w * (n / kWarps) + min(w, n % kWarps); };
   const int ta = split(TU, warp), tb = split(TU, warp + 1);
   const int ra = split(RU, warp), rb = split(RU, warp + 1);
@@ -323,16 +340,19 @@ __global__ void __launch_bounds__(kThreads) gemv_i2s_kernel(const uint8_t* __res
     const int s = issued % g.stages;
     const int n = ic.len();
     uint8_t* dst = ring + size_t(s) * g.stage_bytes;
+    int m;
     if (ic.phase == 0) {
-      const int nrows = min(kRows, tile_rows - ic.idx * kRows);
+      const int t = vsplit(ic.idx, ntile, m);
+      const int nrows = min(kRows, tile_rows - t * kRows);
       if (lane == 0) mbar_arrive_expect_tx(&full[s], uint32_t(nrows * n * 32));
       __syncwarp();
       if (lane < kRows && ir < nrows)
-        bulk_g2s(dst + size_t(ir) * g.rowstride, packed + int64_t(r0 + ic.idx * kRows + ir) * row_bytes + 32 * ic.gg,
+        bulk_g2s(dst + size_t(ir) * g.rowstride, pk(m) + int64_t(r0 + t * kRows + ir) * row_bytes + 32 * ic.gg,
                  uint32_t(n * 32), &full[s], policy_evict_first());
     } else if (lane == 0) {
+      const int j = vsplit(ic.idx, nextra, m);
       mbar_arrive_expect_tx(&full[s], uint32_t(n * 32));
-      bulk_g2s(dst, packed + int64_t(r0 + tile_rows + ic.idx) * row_bytes + 32 * ic.gg, uint32_t(n * 32), &full[s],
+      bulk_g2s(dst, pk(m) + int64_t(r0 + tile_rows + j) * row_bytes + 32 * ic.gg, uint32_t(n * 32), &full[s],
                policy_evict_first());
     }
     ic.advance(n);
@@ -340,7 +360,7 @@ __global__ void __launch_bounds__(kThreads) gemv_i2s_kernel(const uint8_t* __res
   };
 
   if (g.resident) {
-    if (threadIdx.x <= ntile) mbar_init(&full[threadIdx.x], 1);
+    if (int(threadIdx.x) < NM * nbar) mbar_init(&full[threadIdx.x], 1);
   } else if (lane == 0) {
     for (int s = 0; s < g.stages; ++s) mbar_init(&full[s], 1);
   }
@@ -356,14 +376,15 @@ __global__ void __launch_bounds__(kThreads) gemv_i2s_kernel(const uint8_t* __res
   // resident mode: one bulk copy per row of the CTA, tile i completing on
   // barrier i and the single rows on barrier ntile
   auto issue_rows = [&]() {
-    if (threadIdx.x <= ntile) {
-      const int nr = threadIdx.x < ntile ? min(kRows, tile_rows - int(threadIdx.x) * kRows) : nextra;
+    if (int(threadIdx.x) < NM * nbar) {
+      const int b = int(threadIdx.x) % nbar;
+      const int nr = b < ntile ? min(kRows, tile_rows - b * kRows) : nextra;
       mbar_arrive_expect_tx(&full[threadIdx.x], uint32_t(nr) * uint32_t(row_bytes));
     }
-    if (int(threadIdx.x) < rows) {
-      const int t = threadIdx.x;
-      bulk_g2s(ring + size_t(t) * g.rowstride, packed + int64_t(r0 + t) * row_bytes, uint32_t(row_bytes),
-               &full[t < tile_rows ? t / kRows : ntile], policy_evict_first());
+    if (int(threadIdx.x) < NM * rows) {
+      const int m = int(threadIdx.x) / rows, t = int(threadIdx.x) % rows;
+      bulk_g2s(ring + m * mat_bytes + size_t(t) * g.rowstride, pk(m) + int64_t(r0 + t) * row_bytes,
+               uint32_t(row_bytes), &full[m * nbar + (t < tile_rows ? t / kRows : ntile)], policy_evict_first());
     }
   };
   if (early_weights) {
@@ -381,7 +402,17 @@ __global__ void __launch_bounds__(kThreads) gemv_i2s_kernel(const uint8_t* __res
   }
   const bool xvec = (reinterpret_cast<uintptr_t>(x) & 15) == 0;
   prepare_x<D, XB>(x, xvec, g.nC, xrec, warp, lane);
-  const float wscale = *reinterpret_cast<const float*>(packed + int64_t(g.N) * row_bytes);
+  const float wsc0 = *reinterpret_cast<const float*>(pk(0) + int64_t(g.N) * row_bytes);
+  const float wsc1 = NM == 2 ? *reinterpret_cast<const float*>(pk(1) + int64_t(g.N) * row_bytes) : wsc0;
+  float* res = reinterpret_cast<float*>(smem + g.off_res);  // NM == 2: [2][rows_alloc] scaled results
+  // a row's final value: stored (NM == 1) or kept for the epilogue (NM == 2)
+  auto emit = [&](int m, int row_local, float v) {
+    if (NM == 1) {
+      if (!abort_flag) store_y<YB>(y, r0 + row_local, v * wsc0);
+    } else {
+      res[m * g.rows_alloc + row_local] = v * (m ? wsc1 : wsc0);
+    }
+  };
   __syncthreads();
   pdl_launch_dependents();
 
@@ -395,15 +426,18 @@ __global__ void __launch_bounds__(kThreads) gemv_i2s_kernel(const uint8_t* __res
     const int n = cc.len();
     const int phase = cc.phase, idx = cc.idx, gg = cc.gg;
     const int seg_lo = max(phase == 0 ? ta : ra, idx * g.nC);
+    int m;
+    const int loc = vsplit(idx, phase == 0 ? ntile : nextra, m);  // tile or single row within matrix m
     if (g.resident) {
-      if (!abort_flag && !mbar_wait_bounded(&full[phase == 0 ? idx : ntile], 0, g.err)) abort_flag = 1;
+      if (!abort_flag && !mbar_wait_bounded(&full[m * nbar + (phase == 0 ? loc : ntile)], 0, g.err)) abort_flag = 1;
     } else if (!abort_flag && !mbar_wait_bounded(&full[s], uint32_t(i / g.stages) & 1u, g.err)) {
       abort_flag = 1;
     }
     __syncwarp();
     // this chunk's bytes: group gg of the first row (+32 per group, + rowstride per row)
-    const uint8_t* buf = g.resident ? ring + size_t(phase == 0 ? idx * kRows : tile_rows + idx) * g.rowstride + 32 * gg
-                                    : ring + size_t(s) * g.stage_bytes;
+    const uint8_t* buf = g.resident
+                             ? ring + m * mat_bytes + size_t(phase == 0 ? loc * kRows : tile_rows + loc) * g.rowstride + 32 * gg
+                             : ring + size_t(s) * g.stage_bytes;
     if (phase == 0) {
       const uint8_t* rowa = buf + size_t(q) * g.rowstride;
       const uint8_t* rowb = rowa + size_t(8) * g.rowstride;
@@ -441,13 +475,11 @@ __global__ void __launch_bounds__(kThreads) gemv_i2s_kernel(const uint8_t* __res
       float vb = yacc2 + __shfl_xor_sync(0xffffffffu, yacc2, 8);
       va += __shfl_xor_sync(0xffffffffu, va, 16);
       vb += __shfl_xor_sync(0xffffffffu, vb, 16);
-      const int nrows = min(kRows, tile_rows - idx * kRows);
+      const int nrows = min(kRows, tile_rows - loc * kRows);
       if (u == 0) {
         if (whole) {
-          if (!abort_flag) {
-            if (q < nrows) store_y<YB>(y, r0 + idx * kRows + q, va * wscale);
-            if (q + 8 < nrows) store_y<YB>(y, r0 + idx * kRows + q + 8, vb * wscale);
-          }
+          if (q < nrows) emit(m, loc * kRows + q, va);
+          if (q + 8 < nrows) emit(m, loc * kRows + q + 8, vb);
         } else {
           part_t[(warp * 2 + kind) * kRows + q] = va;
           part_t[(warp * 2 + kind) * kRows + q + 8] = vb;
@@ -457,7 +489,7 @@ __global__ void __launch_bounds__(kThreads) gemv_i2s_kernel(const uint8_t* __res
       const float v = warp_sum(yacc);
       if (lane == 0) {
         if (whole) {
-          if (!abort_flag) store_y<YB>(y, r0 + tile_rows + idx, v * wscale);
+          emit(m, tile_rows + loc, v);
         } else {
           part_r[warp * 2 + kind] = v;
         }
@@ -499,16 +531,29 @@ __global__ void __launch_bounds__(kThreads) gemv_i2s_kernel(const uint8_t* __res
 #pragma unroll
           for (int w2 = 0; w2 < kWarps; ++w2) acc += v[w2];
         }
-        const int nrows = min(kRows, tile_rows - t * kRows);
-        if (lane < nrows && !abort_flag) store_y<YB>(y, r0 + t * kRows + lane, acc * wscale);
+        int m;
+        const int tl = vsplit(t, ntile, m);
+        const int nrows = min(kRows, tile_rows - tl * kRows);
+        if (lane < nrows) emit(m, tl * kRows + lane, acc);
       } else if (lane == 0) {
         float v[kWarps];
 #pragma unroll
         for (int w2 = 0; w2 < kWarps; ++w2) v[w2] = (touch >> w2) & 1u ? part_r[w2 * 2 + (w2 == warp ? k : 0)] : 0.f;
 #pragma unroll
         for (int w2 = 0; w2 < kWarps; ++w2) acc += v[w2];
-        if (!abort_flag) store_y<YB>(y, r0 + tile_rows + t, acc * wscale);
+        int m;
+        const int j = vsplit(t, nextra, m);
+        emit(m, tile_rows + j, acc);
       }
+    }
+  }
+
+  if (NM == 2) {
+    // epilogue of the fused gate/up product: h = max(0, g)^2 * u
+    __syncthreads();
+    for (int i = threadIdx.x; i < rows; i += kThreads) {
+      const float gv = fmaxf(res[i], 0.f), uv = res[g.rows_alloc + i];
+      if (!abort_flag) store_y<YB>(y, r0 + i, (gv * gv) * uv);
     }
   }
 
@@ -516,14 +561,14 @@ __global__ void __launch_bounds__(kThreads) gemv_i2s_kernel(const uint8_t* __res
     // let copies still in flight land (bounded) before the CTA exits
     if (g.resident) {
       if (warp == 0)
-        for (int j = 0; j <= ntile; ++j) mbar_wait_bounded(&full[j], 0, nullptr);
+        for (int j = 0; j < NM * nbar; ++j) mbar_wait_bounded(&full[j], 0, nullptr);
     } else {
       for (int j = 0; j < g.stages && j < issued; ++j) mbar_wait_bounded(&full[j], 0, nullptr);
     }
   }
 }
 
-template <int D>
+template <int D, int NM>
 bool plan(Geom& g, int64_t N, int64_t K, int max_smem, int nsm) {
   auto up = [](uint64_t v, uint64_t a) { return (v + a - 1) / a * a; };
   g.N = int(N);
@@ -532,37 +577,42 @@ bool plan(Geom& g, int64_t N, int64_t K, int max_smem, int nsm) {
   g.grid = int(std::min<int64_t>(nsm, N));
   g.q = g.N / g.grid;
   g.rem = g.N % g.grid;
-  // units per warp at most: the tiles of q+1 rows, or a partial tile
+  // units per warp at most: the tiles of q+1 rows (or a partial tile) and a
+  // few single rows, for each matrix
   const int rows = g.q + (g.rem ? 1 : 0);
   const int tiles = (rows + kRows - 1) / kRows;
-  const long long per_warp = ((long long)tiles * g.nC + kWarps - 1) / kWarps + (long long)kExtraMax * g.nC / kWarps + 1;
+  g.tiles_max = tiles;
+  g.rows_alloc = tiles * kRows + kExtraMax;
+  const long long per_warp =
+      NM * (((long long)tiles * g.nC + kWarps - 1) / kWarps + (long long)kExtraMax * g.nC / kWarps + 1);
   const uint64_t fixed_x = up(4ull * g.nC * Rec<D>::kWords, 128);
+  const uint64_t res_bytes = NM == 2 ? up(4ull * 2 * g.rows_alloc, 128) : 0;
   {
     // resident mode when the CTA's rows fit next to the activation records,
     // leaving room for a second CTA (the next kernel's) on the SM
     int rs = int(up(uint64_t(K / 4), 16));
     if (((rs / 16) & 1) == 0) rs += 16;
-    const int tiles_max = tiles;
-    const uint64_t rows_alloc = uint64_t(tiles_max) * kRows + kExtraMax;
     uint64_t off = 0;
     const uint32_t off_bar = uint32_t(off);
-    off = up(off + 8ull * (tiles_max + 1), 128);
+    off = up(off + 8ull * NM * (tiles + 1), 128);
     const uint32_t off_stage = uint32_t(off);
-    off = up(off + rows_alloc * rs, 128);
+    off = up(off + uint64_t(NM) * g.rows_alloc * rs, 128);
     const uint32_t off_part = uint32_t(off);
     off = up(off + 4ull * kWarps * 2 * (kRows + 1), 128);
+    const uint32_t off_res = uint32_t(off);
+    off += res_bytes;
     const uint32_t off_x = uint32_t(off);
     off += fixed_x;
-    if (off <= uint64_t(std::min(max_smem, kResidentSmem)) && tiles_max + 1 <= kThreads) {
+    if (off <= uint64_t(std::min(max_smem, kResidentSmem)) && NM * g.rows_alloc <= kThreads) {
       g.resident = 1;
       g.S = g.nC;
       g.stages = 1;
-      g.tiles_max = tiles_max;
       g.rowstride = rs;
       g.stage_bytes = 0;
       g.off_bar = off_bar;
       g.off_stage = off_stage;
       g.off_part = off_part;
+      g.off_res = off_res;
       g.off_x = off_x;
       g.smem = uint32_t(off);
       return true;
@@ -573,7 +623,7 @@ bool plan(Geom& g, int64_t N, int64_t K, int max_smem, int nsm) {
     int rs = int(up(uint64_t(S) * 32, 16));
     if (((rs / 16) & 1) == 0) rs += 16;
     const uint32_t stage_bytes = uint32_t(up(uint64_t(kRows) * rs, 128));
-    const long long chunks = (per_warp + S - 1) / S + 2;  // tile and phase boundaries add a few
+    const long long chunks = (per_warp + S - 1) / S + 2 * NM;  // tile and phase boundaries add a few
     for (int st = int(std::min<long long>(3, std::max<long long>(1, chunks))); st >= 1; --st) {
       uint64_t off = 0;
       const uint32_t off_bar = uint32_t(off);
@@ -582,6 +632,8 @@ bool plan(Geom& g, int64_t N, int64_t K, int max_smem, int nsm) {
       off = up(off + uint64_t(kWarps) * st * stage_bytes, 128);
       const uint32_t off_part = uint32_t(off);
       off = up(off + 4ull * kWarps * 2 * (kRows + 1), 128);
+      const uint32_t off_res = uint32_t(off);
+      off += res_bytes;
       const uint32_t off_x = uint32_t(off);
       off += fixed_x;
       if (off <= uint64_t(max_smem)) {
@@ -592,6 +644,7 @@ bool plan(Geom& g, int64_t N, int64_t K, int max_smem, int nsm) {
         g.off_bar = off_bar;
         g.off_stage = off_stage;
         g.off_part = off_part;
+        g.off_res = off_res;
         g.off_x = off_x;
         g.smem = uint32_t(off);
         return true;
@@ -607,9 +660,10 @@ struct Plan {
   bool ok;
 };
 
-template <int D, bool XB, bool YB>
-cudaError_t run(const uint8_t* packed, const void* x, void* y, int64_t N, int64_t K, cudaStream_t st) {
-  auto kern = gemv_i2s_kernel<D, XB, YB>;
+template <int D, bool XB, bool YB, int NM>
+cudaError_t run(const uint8_t* packed, const uint8_t* packed2, const void* x, void* y, int64_t N, int64_t K,
+                cudaStream_t st) {
+  auto kern = gemv_i2s_kernel<D, XB, YB, NM>;
   static PlanCache<Plan> cache;
   int dev = 0;
   cudaGetDevice(&dev);
@@ -617,7 +671,7 @@ cudaError_t run(const uint8_t* packed, const void* x, void* y, int64_t N, int64_
   if (!cache.get(dev, N, K, &p)) {
     int max_optin = 0;
     cudaDeviceGetAttribute(&max_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-    p.ok = plan<D>(p.g, N, K, max_optin - 1024, sm_count());
+    p.ok = plan<D, NM>(p.g, N, K, max_optin - 1024, sm_count());
     if (!p.ok) return cudaErrorInvalidConfiguration;
     // the cap is a property of the kernel, shared by every shape: raise it to the maximum once
     cudaError_t e = raise_smem_cap(kern, dev, max_optin - 1024);
@@ -626,7 +680,7 @@ cudaError_t run(const uint8_t* packed, const void* x, void* y, int64_t N, int64_
     cache.put(dev, N, K, p);
   }
   const bool pdl = overlap_enabled();
-  return launch(kern, dim3(p.g.grid), dim3(kThreads), p.g.smem, st, pdl, packed, x, y, p.g, pdl ? 1 : 0);
+  return launch(kern, dim3(p.g.grid), dim3(kThreads), p.g.smem, st, pdl, packed, packed2, x, y, p.g, pdl ? 1 : 0);
 }
 
 }  // namespace
@@ -634,8 +688,19 @@ cudaError_t run(const uint8_t* packed, const void* x, void* y, int64_t N, int64_
 cudaError_t launch_gemv_i2s(const uint8_t* packed, const void* x, bl_dtype xt, void* y, bl_dtype yt, int64_t N,
                             int64_t K, cudaStream_t s) {
   const bool xb = xt == BL_BF16, yb = yt == BL_BF16;
-  if (xb) return yb ? run<2, true, true>(packed, x, y, N, K, s) : run<3, true, false>(packed, x, y, N, K, s);
-  return yb ? run<4, false, true>(packed, x, y, N, K, s) : run<4, false, false>(packed, x, y, N, K, s);
+  if (xb)
+    return yb ? run<2, true, true, 1>(packed, packed, x, y, N, K, s) : run<3, true, false, 1>(packed, packed, x, y, N, K, s);
+  return yb ? run<4, false, true, 1>(packed, packed, x, y, N, K, s) : run<4, false, false, 1>(packed, packed, x, y, N, K, s);
+}
+
+cudaError_t launch_gemv_i2s_gate_up(const uint8_t* packed_gate, const uint8_t* packed_up, const void* x, bl_dtype xt,
+                                    void* h, bl_dtype ht, int64_t N, int64_t K, cudaStream_t s) {
+  const bool xb = xt == BL_BF16, hb = ht == BL_BF16;
+  if (xb)
+    return hb ? run<2, true, true, 2>(packed_gate, packed_up, x, h, N, K, s)
+              : run<3, true, false, 2>(packed_gate, packed_up, x, h, N, K, s);
+  return hb ? run<4, false, true, 2>(packed_gate, packed_up, x, h, N, K, s)
+            : run<4, false, false, 2>(packed_gate, packed_up, x, h, N, K, s);
 }
 
 }  // namespace bl

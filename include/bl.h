@@ -179,6 +179,21 @@ bl_status bl_gemv_i2s(const uint8_t* packed, const void* x, bl_dtype xt, void* y
                       bl_stream_t stream);
 
 /*
+ * Fused gate + up + ReLU^2 x mul of the MLP, one token [BL "Fused
+ * Gate+Up+ReLU²×Mul M=1 Kernel"]:
+ *   g[n] = scale_g * sum_j wg[n,j] x[j],   u[n] = scale_u * sum_j wu[n,j] x[j]
+ *   h[n] = max(0, g[n])^2 * u[n]
+ *   packed_gate, packed_up : two i2_s tensors of the same shape [N, K] as
+ *            written by bl_pack_i2s (each with its own trailing scale).
+ *   x : [K] fp32 or bf16 (xt).   h : [N] fp32 or bf16 (ht).
+ * x is read once for both products.  Accuracy: g and u as bl_gemv_i2s
+ * computes them with an fp32 result; h is formed in fp32 and rounded to bf16
+ * if asked.  Requirements as for bl_gemv_i2s; both tensors 16-byte aligned.
+ */
+bl_status bl_gemv_i2s_gate_up(const uint8_t* packed_gate, const uint8_t* packed_up, const void* x, bl_dtype xt,
+                              void* h, bl_dtype ht, int64_t N, int64_t K, bl_stream_t stream);
+
+/*
  * TQ2_0 GEMV, one token [TQ "TQ2_0 Format"]:
  *   y[n] = sum_b d[n,b] * sum_{j<256} w[n,256b+j] x[256b+j].
  *   packed : as written by bl_pack_tq2_0.  x : [K] fp32 or bf16.  y : fp32 [N].

@@ -244,6 +244,34 @@ int orc_gemv_i2s(const uint8_t* packed, const double* x, int64_t N, int64_t K,
 }
 
 /*
+ * Fused gate + up + ReLU^2 x mul for one token ("Hesper/Layers/BitLinear",
+ * "Fused Gate+Up+ReLU²×Mul M=1 Kernel"): with the two i2_s tensors' own
+ * scales,
+ *   g[n] = s_g * sum_e wg[n,e] x[e],   u[n] = s_u * sum_e wu[n,e] x[e],
+ *   h[n] = max(0, g[n])^2 * u[n]                     (fp64 throughout).
+ * cond[r] = 2 max(0,g) |u| cond_g + max(0,g)^2 cond_u: the first-order bound
+ * of h's error when g and u are each off by at most their own cond.
+ */
+int orc_gemv_i2s_gate_up(const uint8_t* packed_gate, const uint8_t* packed_up, const double* x, int64_t N,
+                         int64_t K, const int64_t* rows, int64_t nrows, double* h, double* cond) {
+  if (nrows < 0) return ORC_ERR_SHAPE;
+  double* buf = (double*)malloc(sizeof(double) * 4 * (size_t)(nrows > 0 ? nrows : 1));
+  if (!buf) return ORC_ERR_SHAPE;
+  double *g = buf, *cg = buf + nrows, *u = buf + 2 * nrows, *cu = buf + 3 * nrows;
+  int st = orc_gemv_i2s(packed_gate, x, N, K, rows, nrows, g, cg);
+  if (st == ORC_OK) st = orc_gemv_i2s(packed_up, x, N, K, rows, nrows, u, cu);
+  if (st == ORC_OK) {
+    for (int64_t r = 0; r < nrows; ++r) {
+      const double a = g[r] > 0.0 ? g[r] : 0.0;
+      h[r] = a * a * u[r];
+      if (cond) cond[r] = 2.0 * a * fabs(u[r]) * cg[r] + a * a * cu[r];
+    }
+  }
+  free(buf);
+  return st;
+}
+
+/*
  * Large-M product with int8 activations:
  *   acc[m,r] = sum_k q[m,k] w[n,k]   (exact, int64)
  *   y[m,r]   = acc[m,r] * s_act[m] * s_w   (fp64)

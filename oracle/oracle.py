@@ -35,6 +35,7 @@ def load(path):
         "orc_pack_i2s": ([p, ctypes.c_float, i64, i64, p], ctypes.c_int),
         "orc_unpack_i2s": ([p, i64, i64, p, p], ctypes.c_int),
         "orc_gemv_i2s": ([p, p, i64, i64, p, i64, p, p], ctypes.c_int),
+        "orc_gemv_i2s_gate_up": ([p, p, p, i64, i64, p, i64, p, p], ctypes.c_int),
         "orc_gemm_i2s_int8": ([p, p, p, i64, i64, i64, p, i64, p, p, p], ctypes.c_int),
         "orc_tq2_0_packed_bytes": ([i64, i64], i64),
         "orc_pack_tq2_0": ([p, p, i64, i64, p], ctypes.c_int),
@@ -140,6 +141,19 @@ def gemv_i2s(packed, x, N, K, rows=None):
     c = np.empty(nr, np.float64)
     _check(lib().orc_gemv_i2s(_ptr(p), _ptr(x), N, K, _ptr(r), nr, _ptr(y), _ptr(c)), "gemv_i2s")
     return y, c
+
+
+def gemv_i2s_gate_up(packed_gate, packed_up, x, N, K, rows=None):
+    """h = max(0, g)^2 * u with g, u the two i2_s GEMVs; returns (h, cond)."""
+    pg = _c(packed_gate, np.uint8)
+    pu = _c(packed_up, np.uint8)
+    x = _c(x, np.float64)
+    r, nr = _rows(rows, N)
+    h = np.empty(nr, np.float64)
+    c = np.empty(nr, np.float64)
+    _check(lib().orc_gemv_i2s_gate_up(_ptr(pg), _ptr(pu), _ptr(x), N, K, _ptr(r), nr, _ptr(h), _ptr(c)),
+           "gemv_i2s_gate_up")
+    return h, c
 
 
 def gemm_i2s_int8(q, s_act, packed, N, K, rows=None):

@@ -183,6 +183,55 @@ def pin_i2s_brute_force_quads():
         assert np.array_equal(y, ref), "i2s brute force quads"
 
 
+def pin_i2s_gate_up_worked_example():
+    """Fused gate + up + ReLU^2 x mul ("Hesper/Layers/BitLinear", "Fused
+    Gate+Up+ReLU²×Mul M=1 Kernel"): h = max(0, g)^2 * u with g, u each scaled
+    by its own tensor scale.  Rows built so that with x = 1 the dots are the
+    counts below; expected values worked out by hand:
+      row 0: g = 0.5*6 = 3,   u = 2*(-1) = -2  -> h = 9 * -2 = -18
+      row 1: g = 0.5*(-4) = -2, u = 2*7 = 14   -> h = 0 (ReLU)
+      row 2: g = 0,           u = 2*4 = 8      -> h = 0
+      row 3: g = 0.5*10 = 5,  u = 2*1 = 2      -> h = 25 * 2 = 50
+      row 4: g = 0.5*2 = 1,   u = 2*(-3) = -6  -> h = -6"""
+    K = 128
+
+    def rows_with(counts):
+        w = np.zeros((len(counts), K), np.int8)
+        for i, c in enumerate(counts):
+            if c > 0:
+                w[i, :c] = 1
+            elif c < 0:
+                w[i, :-c] = -1
+        return w
+
+    wg = rows_with([6, -4, 0, 10, 2])
+    wu = rows_with([-1, 7, 4, 1, -3])
+    x = np.ones(K)
+    h, cond = O.gemv_i2s_gate_up(O.pack_i2s(wg, np.float32(0.5)), O.pack_i2s(wu, np.float32(2.0)), x, 5, K)
+    assert np.array_equal(h, [-18.0, 0.0, 0.0, 50.0, -6.0]), "gate_up worked example: %s" % h
+    # cond: 2 a |u| cond_g + a^2 cond_u with cond_g = 0.5*|count_g|, cond_u = 2*|count_u|
+    assert np.allclose(cond, [2 * 3 * 2 * 3 + 9 * 2, 0, 0, 2 * 5 * 2 * 5 + 25 * 2, 2 * 1 * 6 * 1 + 1 * 6]), cond
+
+
+def pin_i2s_gate_up_composition():
+    """On random inputs the fused result equals the two pinned GEMVs composed
+    through numpy, row selection included."""
+    g = np.random.Generator(np.random.PCG64(41))
+    N, K = 9, 384
+    wg = g.integers(-1, 2, size=(N, K), dtype=np.int8)
+    wu = g.integers(-1, 2, size=(N, K), dtype=np.int8)
+    x = g.standard_normal(K)
+    pg, pu = O.pack_i2s(wg, np.float32(1.5)), O.pack_i2s(wu, np.float32(0.75))
+    yg, _ = O.gemv_i2s(pg, x, N, K)
+    yu, _ = O.gemv_i2s(pu, x, N, K)
+    ref = np.maximum(yg, 0.0) ** 2 * yu
+    h, _ = O.gemv_i2s_gate_up(pg, pu, x, N, K)
+    assert np.allclose(h, ref, rtol=1e-13, atol=1e-12), "gate_up vs composition"
+    rows = np.array([8, 1, 4])
+    h2, _ = O.gemv_i2s_gate_up(pg, pu, x, N, K, rows=rows)
+    assert np.allclose(h2, ref[rows], rtol=1e-13, atol=1e-12), "gate_up row selection"
+
+
 def pin_i2s_int8_gemm():
     """acc = q W^T exactly (numpy int64 matmul); y = acc * s_act * s_w."""
     g = np.random.Generator(np.random.PCG64(13))

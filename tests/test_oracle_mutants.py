@@ -30,6 +30,13 @@ MUTANTS = {
     "i2s_int8_q_transposed": [("acc += (int64_t)q[m * K + k] * w;", "acc += (int64_t)q[k * M + m] * w;")],
     "i2s_int8_dropped_token_scale": [("y[m * nrows + r] = (double)acc * sm * sw;",
                                       "y[m * nrows + r] = (double)acc * sw;")],
+    "gate_up_relu_on_up": [("const double a = g[r] > 0.0 ? g[r] : 0.0;\n      h[r] = a * a * u[r];",
+                            "const double a = g[r];\n      h[r] = a * a * (u[r] > 0.0 ? u[r] : 0.0);")],
+    "gate_up_not_squared": [("h[r] = a * a * u[r];", "h[r] = a * u[r];")],
+    "gate_up_scales_swapped": [("int st = orc_gemv_i2s(packed_gate, x, N, K, rows, nrows, g, cg);",
+                                "int st = orc_gemv_i2s(packed_up, x, N, K, rows, nrows, g, cg);"),
+                               ("if (st == ORC_OK) st = orc_gemv_i2s(packed_up, x, N, K, rows, nrows, u, cu);",
+                                "if (st == ORC_OK) st = orc_gemv_i2s(packed_gate, x, N, K, rows, nrows, u, cu);")],
     "tq2_decode_sign": [("{0, 1, 99, -1}", "{0, -1, 99, 1}")],
     "tq2_shift_order_both_ways": [("return tq2_value_of((blk[j / 4] >> (2 * (j % 4))) & 3);",
                                    "return tq2_value_of((blk[j / 4] >> (6 - 2 * (j % 4))) & 3);"),

@@ -192,6 +192,57 @@ def test_gemv_i2s_workload_mlp(B, mat):
 
 
 # ---------------------------------------------------------------------------
+# fused gate + up + ReLU^2 x mul
+# ---------------------------------------------------------------------------
+
+def run_gate_up(B, wg, wu, sg, su, x, xd, hd):
+    N, K = wg.shape
+    pg, pu = B.bl_pack_i2s(to_gpu(wg), sg), B.bl_pack_i2s(to_gpu(wu), su)
+    h = B.bl_gemv_i2s_gate_up(pg, pu, x_gpu(x, xd), N, K, h_dtype=torch.float32 if hd == "f32" else torch.bfloat16)
+    hv = h.cpu().numpy().astype(np.float64) if hd == "f32" else x_f64(bits16(h), "bf16")
+    ref, cond = O.gemv_i2s_gate_up(O.pack_i2s(wg, sg), O.pack_i2s(wu, su), x_f64(x, xd), N, K)
+    return hv, ref, cond
+
+
+@pytest.mark.parametrize("xd,hd", [("f32", "f32"), ("bf16", "bf16"), ("bf16", "f32"), ("f32", "bf16")])
+@pytest.mark.parametrize("N,K", [(1, 128), (7, 256), (33, 2560), (100, 1024), (257, 6912), (20, 32768)])
+def test_gemv_i2s_gate_up_small(B, xd, hd, N, K):
+    g = rng(3 * N + K)
+    wg, wu = ternary(g, N, K), ternary(g, N, K)
+    x = rand_x(g, K, xd)
+    h, ref, cond = run_gate_up(B, wg, wu, np.float32(g.uniform(0.5, 2)), np.float32(g.uniform(0.5, 2)), x, xd, hd)
+    assert_close(h, ref, cond, TOL_F32 if hd == "f32" else TOL_BF16, "gate_up %dx%d %s->%s" % (N, K, xd, hd))
+
+
+def test_gemv_i2s_gate_up_workload(B):
+    """BitNet-2B MLP gate/up shapes (6912 x 2560), bf16 in/out, all rows."""
+    wl = synth.WORKLOADS["i2s_mlp_bitnet2b"]
+    N, K = wl.extra["gate"]
+    wg = synth.weight_matrix(wl.index, "w_gate", N, K, "ternary", wl.p_zero)
+    wu = synth.weight_matrix(wl.index, "w_up", N, K, "ternary", wl.p_zero)
+    x = synth.activations(wl.index, 1, K, "bf16")[0]
+    h, ref, cond = run_gate_up(B, wg, wu, synth.tensor_scale(wl.index, "scale_gate"),
+                               synth.tensor_scale(wl.index, "scale_up"), x, "bf16", "bf16")
+    assert_close(h, ref, cond, TOL_BF16, "gate_up workload")
+
+
+def test_gemv_i2s_gate_up_matches_unfused(B):
+    """With fp32 output the fused product equals relu(g)^2 * u formed on the
+    host from two bl_gemv_i2s results (same per-row arithmetic)."""
+    g = rng(77)
+    N, K = 300, 2560
+    wg, wu = ternary(g, N, K), ternary(g, N, K)
+    x = rand_x(g, K, "f32")
+    pg, pu = B.bl_pack_i2s(to_gpu(wg), np.float32(1.25)), B.bl_pack_i2s(to_gpu(wu), np.float32(0.5))
+    xg = x_gpu(x, "f32")
+    h = B.bl_gemv_i2s_gate_up(pg, pu, xg, N, K, h_dtype=torch.float32).cpu().numpy().astype(np.float64)
+    gv = B.bl_gemv_i2s(pg, xg, N, K, y_dtype=torch.float32).cpu().numpy().astype(np.float64)
+    uv = B.bl_gemv_i2s(pu, xg, N, K, y_dtype=torch.float32).cpu().numpy().astype(np.float64)
+    ref = np.maximum(gv, 0) ** 2 * uv
+    assert np.allclose(h, ref, rtol=1e-5, atol=1e-6 * np.abs(ref).max())
+
+
+# ---------------------------------------------------------------------------
 # TQ2_0 GEMV
 # ---------------------------------------------------------------------------
 
@@ -372,6 +423,12 @@ def test_error_paths(B):
     with pytest.raises(B.BLError) as e:
         B.bl_gemv_i2s(p[1:], x, 4, 128)
     assert e.value.status == B.BL_ERR_ALIGN
+    with pytest.raises(B.BLError) as e:
+        B.bl_gemv_i2s_gate_up(p, p[1:], x, 4, 128)
+    assert e.value.status == B.BL_ERR_ALIGN
+    with pytest.raises(B.BLError) as e:
+        B.bl_gemv_i2s_gate_up(p, p, x, 4, 96)
+    assert e.value.status == B.BL_ERR_SHAPE
     q = torch.zeros((9, 128), dtype=torch.int8, device="cuda")
     with pytest.raises(B.BLError) as e:
         B.bl_gemm_w1a8(q, torch.ones(9, device="cuda"), torch.zeros((4, 4), dtype=torch.int32, device="cuda"),
