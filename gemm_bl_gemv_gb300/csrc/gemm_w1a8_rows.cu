@@ -108,6 +108,9 @@ __global__ void __launch_bounds__(256, (MT <= 4 ? 2 : 1)) gemm_w1a8_rows_kernel(
   const int npre = min(my_tiles, g.stages);
   if (early_weights)
     for (int i = 0; i < npre; ++i) issue(i);
+  // let the next kernel's CTAs become resident now: they fetch their own
+  // weights and then wait for this grid to complete before touching its outputs
+  pdl_launch_dependents();
   pdl_wait();
   if (threadIdx.x == 0) {
     mbar_arrive_expect_tx(qbar, uint32_t(MT * g.K));
@@ -142,7 +145,6 @@ __global__ void __launch_bounds__(256, (MT <= 4 ? 2 : 1)) gemm_w1a8_rows_kernel(
     }
   }
   __syncthreads();
-  pdl_launch_dependents();
 
   const int a = lane & 3, v = lane >> 2;  // row slot, group phase
   for (int i = 0; i < my_tiles; ++i) {

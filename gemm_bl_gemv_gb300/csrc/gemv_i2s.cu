@@ -393,6 +393,9 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_i2s_kernel(const uint8_t* __
     else
       for (int i = 0; i < g.stages; ++i) issue_next();
   }
+  // let the next kernel's CTAs become resident now: they fetch their own
+  // weights and then wait for this grid to complete before touching its outputs
+  pdl_launch_dependents();
   pdl_wait();
   if (!early_weights) {
     if (g.resident)
@@ -414,7 +417,6 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_i2s_kernel(const uint8_t* __
     }
   };
   __syncthreads();
-  pdl_launch_dependents();
 
   // ---- the warp's units, chunk by chunk -------------------------------------
   Cursor cc;

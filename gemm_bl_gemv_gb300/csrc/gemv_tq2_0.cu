@@ -154,6 +154,9 @@ __global__ void __launch_bounds__(256) gemv_tq2_0_kernel(const uint8_t* __restri
   const int npre = min(my_tiles, g.stages);
   if (early_weights && lane == 0)
     for (int i = 0; i < npre; ++i) issue(i);
+  // let the next kernel's CTAs become resident now: they fetch their own
+  // weights and then wait for this grid to complete before touching its outputs
+  pdl_launch_dependents();
   pdl_wait();
   const bool x_bulk = (reinterpret_cast<uintptr_t>(x) & 15) == 0;
   if (threadIdx.x == 0 && x_bulk) {
@@ -171,7 +174,6 @@ __global__ void __launch_bounds__(256) gemv_tq2_0_kernel(const uint8_t* __restri
   }
   prepare_x<D, XB>(xraw, g.nb, xrec, warp, nwarps, lane);
   __syncthreads();
-  pdl_launch_dependents();
 
   for (int i = 0; i < my_tiles; ++i) {
     const int st = i % g.stages;
