@@ -21,7 +21,7 @@ BL_DEVERR_WAIT_TIMEOUT = 0x1
 EXPORTS = [
     "bl_status_string", "bl_last_error", "bl_device_error", "bl_set_overlap", "bl_get_overlap",
     "bl_pack_i2s", "bl_pack_tq2_0", "bl_pack_w1", "bl_quantize_act_absmax_int8",
-    "bl_gemv_i2s", "bl_gemv_i2s_gate_up", "bl_gemv_tq2_0", "bl_gemm_w1a8", "bl_gemm_i2s_int8",
+    "bl_gemv_i2s", "bl_gemv_i2s_residual", "bl_gemv_i2s_rmsnorm", "bl_gemv_i2s_gate_up", "bl_gemv_tq2_0", "bl_gemm_w1a8", "bl_gemm_i2s_int8",
 ]
 
 
@@ -45,6 +45,8 @@ def _declare(L):
         "bl_quantize_act_absmax_int8": ([p, i32, i64, i64, p, p, p], st),
         "bl_gemv_i2s": ([p, p, i32, p, i32, i64, i64, p], st),
         "bl_gemv_i2s_gate_up": ([p, p, p, i32, p, i32, i64, i64, p], st),
+        "bl_gemv_i2s_residual": ([p, p, i32, p, p, i32, i64, i64, p], st),
+        "bl_gemv_i2s_rmsnorm": ([p, p, i32, p, ctypes.c_float, p, p, i32, i64, i64, p], st),
         "bl_gemv_tq2_0": ([p, p, i32, p, i64, i64, p], st),
         "bl_gemm_w1a8": ([p, p, p, p, p, i64, i64, i64, i32, p, p, p], st),
         "bl_gemm_i2s_int8": ([p, p, p, i64, i64, i64, p, p, p], st),
@@ -178,6 +180,39 @@ def bl_gemv_i2s(packed, x, N, K, y=None, y_dtype=None, stream=None):
         y = torch.empty(N, dtype=y_dtype or x.dtype, device=x.device)
     _check(_lib.bl_gemv_i2s(_ptr(packed), _ptr(x), _dtype_code(x), _ptr(_cuda(y, "y")), _dtype_code(y), N, K,
                             _stream(stream)))
+    return y
+
+
+def bl_gemv_i2s_residual(packed, x, residual, N, K, y=None, stream=None):
+    """y = residual + scale * W x (y and residual share a dtype)."""
+    _cuda(packed, "packed")
+    _cuda(x, "x")
+    _cuda(residual, "residual")
+    if y is None:
+        y = torch.empty(N, dtype=residual.dtype, device=x.device)
+    if y.dtype != residual.dtype:
+        raise TypeError("y and residual must share a dtype")
+    _check(_lib.bl_gemv_i2s_residual(_ptr(packed), _ptr(x), _dtype_code(x), _ptr(residual), _ptr(_cuda(y, "y")),
+                                     _dtype_code(y), N, K, _stream(stream)))
+    return y
+
+
+def bl_gemv_i2s_rmsnorm(packed, x, rms_weight, N, K, eps=1e-5, residual=None, y=None, y_dtype=None, stream=None):
+    """y = residual + scale * W (x * rmsInv * rms_weight), rmsInv = 1/sqrt(mean(x^2) + eps)."""
+    _cuda(packed, "packed")
+    _cuda(x, "x")
+    _cuda(rms_weight, "rms_weight")
+    if rms_weight.dtype != x.dtype:
+        raise TypeError("rms_weight must have x's dtype")
+    if y is None:
+        y = torch.empty(N, dtype=(residual.dtype if residual is not None else (y_dtype or x.dtype)), device=x.device)
+    if residual is not None:
+        _cuda(residual, "residual")
+        if residual.dtype != y.dtype:
+            raise TypeError("y and residual must share a dtype")
+    _check(_lib.bl_gemv_i2s_rmsnorm(_ptr(packed), _ptr(x), _dtype_code(x), _ptr(rms_weight), float(eps),
+                                    _ptr(residual) if residual is not None else None, _ptr(_cuda(y, "y")),
+                                    _dtype_code(y), N, K, _stream(stream)))
     return y
 
 

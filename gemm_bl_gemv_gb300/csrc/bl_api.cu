@@ -172,6 +172,43 @@ bl_status bl_gemv_i2s(const uint8_t* packed, const void* x, bl_dtype xt, void* y
   return cuda_status(launch_gemv_i2s(packed, x, xt, y, yt, N, K, S(stream)), "bl_gemv_i2s");
 }
 
+static bl_status check_gemv_i2s(const char* fn, const uint8_t* packed, const void* x, bl_dtype xt, const void* y,
+                                bl_dtype yt, int64_t N, int64_t K) {
+  if (!packed || !x || !y) return fail(BL_ERR_NULL, "%s: NULL pointer", fn);
+  if ((xt != BL_F32 && xt != BL_BF16) || (yt != BL_F32 && yt != BL_BF16))
+    return fail(BL_ERR_DTYPE, "%s: bad dtype (x %d, y %d)", fn, int(xt), int(yt));
+  if (N < 1 || K < 128 || K % 128 || N > 0x7fffffff)
+    return fail(BL_ERR_SHAPE, "%s: need N >= 1, K %% 128 == 0 (N=%lld K=%lld)", fn, (long long)N, (long long)K);
+  if (K > 32768) return fail(BL_ERR_UNSUPPORTED, "%s: K up to 32768 supported (K=%lld)", fn, (long long)K);
+  if (!aligned(packed, 16)) return fail(BL_ERR_ALIGN, "%s: packed must be 16-byte aligned", fn);
+  if (!aligned(x, xt == BL_F32 ? 4 : 2) || !aligned(y, yt == BL_F32 ? 4 : 2))
+    return fail(BL_ERR_ALIGN, "%s: x and y must be aligned to their element size", fn);
+  return BL_OK;
+}
+
+bl_status bl_gemv_i2s_residual(const uint8_t* packed, const void* x, bl_dtype xt, const void* residual, void* y,
+                               bl_dtype yt, int64_t N, int64_t K, bl_stream_t stream) {
+  const bl_status st = check_gemv_i2s("bl_gemv_i2s_residual", packed, x, xt, y, yt, N, K);
+  if (st != BL_OK) return st;
+  if (!residual) return fail(BL_ERR_NULL, "bl_gemv_i2s_residual: residual is NULL");
+  if (!aligned(residual, yt == BL_F32 ? 4 : 2))
+    return fail(BL_ERR_ALIGN, "bl_gemv_i2s_residual: residual must be aligned to its element size");
+  return cuda_status(launch_gemv_i2s(packed, x, xt, y, yt, N, K, S(stream), residual, nullptr, 0.f),
+                     "bl_gemv_i2s_residual");
+}
+
+bl_status bl_gemv_i2s_rmsnorm(const uint8_t* packed, const void* x, bl_dtype xt, const void* rms_weight, float eps,
+                              const void* residual, void* y, bl_dtype yt, int64_t N, int64_t K, bl_stream_t stream) {
+  const bl_status st = check_gemv_i2s("bl_gemv_i2s_rmsnorm", packed, x, xt, y, yt, N, K);
+  if (st != BL_OK) return st;
+  if (!rms_weight) return fail(BL_ERR_NULL, "bl_gemv_i2s_rmsnorm: rms_weight is NULL");
+  if (!aligned(rms_weight, xt == BL_F32 ? 4 : 2) || (residual && !aligned(residual, yt == BL_F32 ? 4 : 2)))
+    return fail(BL_ERR_ALIGN, "bl_gemv_i2s_rmsnorm: rms_weight / residual must be aligned to their element size");
+  if (!(eps >= 0.f)) return fail(BL_ERR_SHAPE, "bl_gemv_i2s_rmsnorm: eps must be >= 0");
+  return cuda_status(launch_gemv_i2s(packed, x, xt, y, yt, N, K, S(stream), residual, rms_weight, eps),
+                     "bl_gemv_i2s_rmsnorm");
+}
+
 bl_status bl_gemv_i2s_gate_up(const uint8_t* packed_gate, const uint8_t* packed_up, const void* x, bl_dtype xt,
                               void* h, bl_dtype ht, int64_t N, int64_t K, bl_stream_t stream) {
   if (!packed_gate || !packed_up || !x || !h) return fail(BL_ERR_NULL, "bl_gemv_i2s_gate_up: NULL pointer");

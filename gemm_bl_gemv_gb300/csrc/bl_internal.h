@@ -83,8 +83,10 @@ cudaError_t launch_pack_i2s(const int8_t* w, float scale, int64_t N, int64_t K, 
 cudaError_t launch_pack_tq2_0(const int8_t* w, const uint16_t* d, int64_t N, int64_t K, uint8_t* out, cudaStream_t s);
 cudaError_t launch_pack_w1(const int8_t* w, int64_t N, int64_t K, int32_t* out, cudaStream_t s);
 cudaError_t launch_act_quant(const void* x, bl_dtype xt, int64_t M, int64_t K, int8_t* q, float* sc, cudaStream_t s);
+// residual (y's dtype, [N]) and rms_w (x's dtype, [K]) may be nullptr
 cudaError_t launch_gemv_i2s(const uint8_t* packed, const void* x, bl_dtype xt, void* y, bl_dtype yt, int64_t N,
-                            int64_t K, cudaStream_t s);
+                            int64_t K, cudaStream_t s, const void* residual = nullptr, const void* rms_w = nullptr,
+                            float eps = 0.f);
 cudaError_t launch_gemv_i2s_gate_up(const uint8_t* packed_gate, const uint8_t* packed_up, const void* x, bl_dtype xt,
                                     void* h, bl_dtype ht, int64_t N, int64_t K, cudaStream_t s);
 cudaError_t launch_gemv_tq2_0(const uint8_t* packed, const void* x, bl_dtype xt, float* y, int64_t N, int64_t K,

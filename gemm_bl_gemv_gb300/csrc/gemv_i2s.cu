@@ -76,6 +76,11 @@ struct Geom {
   uint32_t stage_bytes;
   uint32_t off_bar, off_stage, off_part, off_res, off_x, smem;
   unsigned int* err;
+  // per call (single matrix only): residual added to y (y's dtype) and
+  // RMSNorm weights (x's dtype) with epsilon; nullptr when not used
+  const void* residual;
+  const void* rms_w;
+  float eps;
 };
 
 // Per-group activation record: [8 words][4 shifts][D digits] u32, then D
@@ -153,13 +158,22 @@ __device__ __forceinline__ void prep_group(const float (&v)[4], uint32_t* rec, i
 // Records of all nC groups, warp w taking groups w, w+16, ...; the loads of
 // up to four groups are in flight together.
 template <int D, bool XB>
-__device__ __forceinline__ void prepare_x(const void* x, bool vec, int nC, uint32_t* xrec, int warp, int lane) {
+__device__ __forceinline__ void prepare_x(const void* x, bool vec, int nC, uint32_t* xrec, int warp, int lane,
+                                          const void* rmsw, bool wvec, float rinv) {
   constexpr int RW = Rec<D>::kWords;
   for (int c0 = warp; c0 < nC; c0 += 4 * kWarps) {
     float v[4][4];
 #pragma unroll
     for (int b = 0; b < 4; ++b)
-      if (c0 + b * kWarps < nC) load4<XB>(x, vec, (c0 + b * kWarps) * 128 + 4 * lane, v[b]);
+      if (c0 + b * kWarps < nC) {
+        load4<XB>(x, vec, (c0 + b * kWarps) * 128 + 4 * lane, v[b]);
+        if (rmsw) {  // RMSNorm: x * rmsInv * weight
+          float w[4];
+          load4<XB>(rmsw, wvec, (c0 + b * kWarps) * 128 + 4 * lane, w);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) v[b][i] = __fmul_rn(__fmul_rn(v[b][i], rinv), w[i]);
+        }
+      }
 #pragma unroll
     for (int b = 0; b < 4; ++b)
       if (c0 + b * kWarps < nC) prep_group<D>(v[b], xrec + (c0 + b * kWarps) * RW, lane);
@@ -404,14 +418,41 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_i2s_kernel(const uint8_t* __
       for (int i = 0; i < g.stages; ++i) issue_next();
   }
   const bool xvec = (reinterpret_cast<uintptr_t>(x) & 15) == 0;
-  prepare_x<D, XB>(x, xvec, g.nC, xrec, warp, lane);
+  float rinv = 1.f;
+  if (NM == 1 && g.rms_w) {
+    // RMSNorm factor 1 / sqrt(mean(x^2) + eps): lanes, warps and the CTA sum
+    // in a fixed order (every CTA gets the same value)
+    __shared__ float ssq[kWarps];
+    float part = 0.f;
+    for (int c0 = warp; c0 < g.nC; c0 += kWarps) {
+      float v[4];
+      load4<XB>(x, xvec, c0 * 128 + 4 * lane, v);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) part = __fadd_rn(part, __fmul_rn(v[i], v[i]));
+    }
+    part = warp_sum(part);
+    if (lane == 0) ssq[warp] = part;
+    __syncthreads();
+    float tot = 0.f;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) tot = __fadd_rn(tot, ssq[w]);
+    rinv = __fdiv_rn(1.f, __fsqrt_rn(__fadd_rn(__fdiv_rn(tot, float(g.K)), g.eps)));
+  }
+  prepare_x<D, XB>(x, xvec, g.nC, xrec, warp, lane, NM == 1 ? g.rms_w : nullptr,
+                   (reinterpret_cast<uintptr_t>(g.rms_w) & 15) == 0, rinv);
   const float wsc0 = *reinterpret_cast<const float*>(pk(0) + int64_t(g.N) * row_bytes);
   const float wsc1 = NM == 2 ? *reinterpret_cast<const float*>(pk(1) + int64_t(g.N) * row_bytes) : wsc0;
   float* res = reinterpret_cast<float*>(smem + g.off_res);  // NM == 2: [2][rows_alloc] scaled results
   // a row's final value: stored (NM == 1) or kept for the epilogue (NM == 2)
   auto emit = [&](int m, int row_local, float v) {
     if (NM == 1) {
-      if (!abort_flag) store_y<YB>(y, r0 + row_local, v * wsc0);
+      float out = v * wsc0;
+      if (g.residual) {
+        const int row = r0 + row_local;
+        out += YB ? bf16_bits_to_f32(reinterpret_cast<const uint16_t*>(g.residual)[row])
+                  : reinterpret_cast<const float*>(g.residual)[row];
+      }
+      if (!abort_flag) store_y<YB>(y, r0 + row_local, out);
     } else {
       res[m * g.rows_alloc + row_local] = v * (m ? wsc1 : wsc0);
     }
@@ -664,7 +705,7 @@ struct Plan {
 
 template <int D, bool XB, bool YB, int NM>
 cudaError_t run(const uint8_t* packed, const uint8_t* packed2, const void* x, void* y, int64_t N, int64_t K,
-                cudaStream_t st) {
+                cudaStream_t st, const void* residual = nullptr, const void* rms_w = nullptr, float eps = 0.f) {
   auto kern = gemv_i2s_kernel<D, XB, YB, NM>;
   static PlanCache<Plan> cache;
   int dev = 0;
@@ -681,6 +722,9 @@ cudaError_t run(const uint8_t* packed, const uint8_t* packed2, const void* x, vo
     p.g.err = dev_error_ptr();
     cache.put(dev, N, K, p);
   }
+  p.g.residual = residual;
+  p.g.rms_w = rms_w;
+  p.g.eps = eps;
   const bool pdl = overlap_enabled();
   return launch(kern, dim3(p.g.grid), dim3(kThreads), p.g.smem, st, pdl, packed, packed2, x, y, p.g, pdl ? 1 : 0);
 }
@@ -688,11 +732,13 @@ cudaError_t run(const uint8_t* packed, const uint8_t* packed2, const void* x, vo
 }  // namespace
 
 cudaError_t launch_gemv_i2s(const uint8_t* packed, const void* x, bl_dtype xt, void* y, bl_dtype yt, int64_t N,
-                            int64_t K, cudaStream_t s) {
+                            int64_t K, cudaStream_t s, const void* residual, const void* rms_w, float eps) {
   const bool xb = xt == BL_BF16, yb = yt == BL_BF16;
   if (xb)
-    return yb ? run<2, true, true, 1>(packed, packed, x, y, N, K, s) : run<3, true, false, 1>(packed, packed, x, y, N, K, s);
-  return yb ? run<4, false, true, 1>(packed, packed, x, y, N, K, s) : run<4, false, false, 1>(packed, packed, x, y, N, K, s);
+    return yb ? run<2, true, true, 1>(packed, packed, x, y, N, K, s, residual, rms_w, eps)
+              : run<3, true, false, 1>(packed, packed, x, y, N, K, s, residual, rms_w, eps);
+  return yb ? run<4, false, true, 1>(packed, packed, x, y, N, K, s, residual, rms_w, eps)
+            : run<4, false, false, 1>(packed, packed, x, y, N, K, s, residual, rms_w, eps);
 }
 
 cudaError_t launch_gemv_i2s_gate_up(const uint8_t* packed_gate, const uint8_t* packed_up, const void* x, bl_dtype xt,

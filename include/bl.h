@@ -179,6 +179,29 @@ bl_status bl_gemv_i2s(const uint8_t* packed, const void* x, bl_dtype xt, void* y
                       bl_stream_t stream);
 
 /*
+ * i2_s GEMV with the residual added [BL "M=1 warp-cooperative kernel with
+ * fused residual add"]:  y[n] = residual[n] + scale * sum_j w[n,j] x[j].
+ *   residual : [N] in y's dtype (yt); may alias y.
+ * Otherwise as bl_gemv_i2s (the sum is formed in fp32, then rounded).
+ */
+bl_status bl_gemv_i2s_residual(const uint8_t* packed, const void* x, bl_dtype xt, const void* residual, void* y,
+                               bl_dtype yt, int64_t N, int64_t K, bl_stream_t stream);
+
+/*
+ * Fused RMSNorm + i2_s GEMV + residual [BL "Fused RMSNorm + BitLinear +
+ * Residual Add M=1 Kernel"]:
+ *   rmsInv = 1 / sqrt(sum_j x[j]^2 / K + eps)
+ *   y[n]   = residual[n] + scale * sum_j w[n,j] * (x[j] * rmsInv * rms_weight[j])
+ *   rms_weight : [K] in x's dtype (xt).   residual : [N] in yt, or NULL (0).
+ * rmsInv is computed in fp32 (fixed summation order, IEEE sqrt and
+ * division); the normalized activations are fp32 and go through the same
+ * per-group fixed-point path as bl_gemv_i2s.  Requirements as for
+ * bl_gemv_i2s; rms_weight aligned to its element size.
+ */
+bl_status bl_gemv_i2s_rmsnorm(const uint8_t* packed, const void* x, bl_dtype xt, const void* rms_weight, float eps,
+                              const void* residual, void* y, bl_dtype yt, int64_t N, int64_t K, bl_stream_t stream);
+
+/*
  * Fused gate + up + ReLU^2 x mul of the MLP, one token [BL "Fused
  * Gate+Up+ReLU²×Mul M=1 Kernel"]:
  *   g[n] = scale_g * sum_j wg[n,j] x[j],   u[n] = scale_u * sum_j wu[n,j] x[j]

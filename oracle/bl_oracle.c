@@ -272,6 +272,37 @@ int orc_gemv_i2s_gate_up(const uint8_t* packed_gate, const uint8_t* packed_up, c
 }
 
 /*
+ * Fused RMSNorm + BitLinear + residual for one token ("Hesper/Layers/BitLinear",
+ * "Fused RMSNorm + BitLinear + Residual Add M=1 Kernel" and the M=1 kernel
+ * with fused residual add), fp64 throughout:
+ *   rmsInv = 1 / sqrt(sum_e x[e]^2 / K + eps)      (when rms_w is given)
+ *   x'[e]  = x[e] * rmsInv * rms_w[e]               (else x' = x)
+ *   y[r]   = residual[n] + s * sum_e w[n,e] x'[e]   (residual may be NULL: 0)
+ * cond[r] = |s| * sum_e |w[n,e]| |x'[e]| (the rounding of the residual sum is
+ * covered by the |y| term of the tolerance).
+ */
+int orc_gemv_i2s_norm_residual(const uint8_t* packed, const double* x, const double* rms_w, double eps,
+                               const double* residual, int64_t N, int64_t K, const int64_t* rows, int64_t nrows,
+                               double* y, double* cond) {
+  if (N < 0 || K <= 0 || K % 128 != 0 || nrows < 0) return ORC_ERR_SHAPE;
+  double* xn = (double*)malloc(sizeof(double) * (size_t)K);
+  if (!xn) return ORC_ERR_SHAPE;
+  double inv = 1.0;
+  if (rms_w) {
+    double ss = 0.0;
+    for (int64_t e = 0; e < K; ++e) ss += x[e] * x[e];
+    inv = 1.0 / sqrt(ss / (double)K + eps);
+  }
+  for (int64_t e = 0; e < K; ++e) xn[e] = rms_w ? x[e] * inv * rms_w[e] : x[e];
+  int st = orc_gemv_i2s(packed, xn, N, K, rows, nrows, y, cond);
+  if (st == ORC_OK && residual) {
+    for (int64_t r = 0; r < nrows; ++r) y[r] += residual[rows ? rows[r] : r];
+  }
+  free(xn);
+  return st;
+}
+
+/*
  * Large-M product with int8 activations:
  *   acc[m,r] = sum_k q[m,k] w[n,k]   (exact, int64)
  *   y[m,r]   = acc[m,r] * s_act[m] * s_w   (fp64)

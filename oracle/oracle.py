@@ -36,6 +36,7 @@ def load(path):
         "orc_unpack_i2s": ([p, i64, i64, p, p], ctypes.c_int),
         "orc_gemv_i2s": ([p, p, i64, i64, p, i64, p, p], ctypes.c_int),
         "orc_gemv_i2s_gate_up": ([p, p, p, i64, i64, p, i64, p, p], ctypes.c_int),
+        "orc_gemv_i2s_norm_residual": ([p, p, p, ctypes.c_double, p, i64, i64, p, i64, p, p], ctypes.c_int),
         "orc_gemm_i2s_int8": ([p, p, p, i64, i64, i64, p, i64, p, p, p], ctypes.c_int),
         "orc_tq2_0_packed_bytes": ([i64, i64], i64),
         "orc_pack_tq2_0": ([p, p, i64, i64, p], ctypes.c_int),
@@ -154,6 +155,22 @@ def gemv_i2s_gate_up(packed_gate, packed_up, x, N, K, rows=None):
     _check(lib().orc_gemv_i2s_gate_up(_ptr(pg), _ptr(pu), _ptr(x), N, K, _ptr(r), nr, _ptr(h), _ptr(c)),
            "gemv_i2s_gate_up")
     return h, c
+
+
+def gemv_i2s_norm_residual(packed, x, N, K, rms_w=None, eps=1e-5, residual=None, rows=None):
+    """y = residual + scale * W (x * rmsInv * rms_w)  (RMSNorm only when rms_w is given,
+    residual 0 when None); returns (y, cond)."""
+    p = _c(packed, np.uint8)
+    x = _c(x, np.float64)
+    w = None if rms_w is None else _c(rms_w, np.float64)
+    res = None if residual is None else _c(residual, np.float64)
+    r, nr = _rows(rows, N)
+    y = np.empty(nr, np.float64)
+    c = np.empty(nr, np.float64)
+    _check(lib().orc_gemv_i2s_norm_residual(_ptr(p), _ptr(x), _ptr(w) if w is not None else None, float(eps),
+                                            _ptr(res) if res is not None else None, N, K, _ptr(r), nr, _ptr(y),
+                                            _ptr(c)), "gemv_i2s_norm_residual")
+    return y, c
 
 
 def gemm_i2s_int8(q, s_act, packed, N, K, rows=None):

@@ -232,6 +232,54 @@ def pin_i2s_gate_up_composition():
     assert np.allclose(h2, ref[rows], rtol=1e-13, atol=1e-12), "gate_up row selection"
 
 
+def pin_i2s_norm_residual_worked_example():
+    """Fused RMSNorm + BitLinear + residual ("Hesper/Layers/BitLinear",
+    "Fused RMSNorm + BitLinear + Residual Add M=1 Kernel"):
+    rmsInv = 1/sqrt(mean(x^2) + eps), x' = x * rmsInv * w_rms, y = res + s W x'.
+    Worked by hand with K = 128, x = 1 everywhere, eps = 3: mean(x^2) = 1,
+    rmsInv = 1/sqrt(4) = 0.5.  w_rms = 2 on elements 0..63, 1 elsewhere, so
+    x' = 1 on 0..63 and 0.5 on 64..127.  Rows (s = 2, residual = 10, -3, 0):
+      row 0: +1 on 0..9              -> dot = 10       -> y = 10 + 20 = 30
+      row 1: +1 on 64..71            -> dot = 4        -> y = -3 + 8  = 5
+      row 2: -1 on 0..3, +1 on 64..67 -> dot = -4 + 2 = -2 -> y = 0 - 4 = -4
+    Without the norm (rms_w None) the same rows give 10, 8, 0 plus residual."""
+    K = 128
+    w = np.zeros((3, K), np.int8)
+    w[0, :10] = 1
+    w[1, 64:72] = 1
+    w[2, :4] = -1
+    w[2, 64:68] = 1
+    x = np.ones(K)
+    rms_w = np.where(np.arange(K) < 64, 2.0, 1.0)
+    res = np.array([10.0, -3.0, 0.0])
+    p = O.pack_i2s(w, np.float32(2.0))
+    y, cond = O.gemv_i2s_norm_residual(p, x, 3, K, rms_w=rms_w, eps=3.0, residual=res)
+    assert np.array_equal(y, [30.0, 5.0, -4.0]), "norm+residual worked example: %s" % y
+    assert np.array_equal(cond, [20.0, 8.0, 12.0]), "norm+residual cond: %s" % cond
+    y2, _ = O.gemv_i2s_norm_residual(p, x, 3, K, residual=res)
+    assert np.array_equal(y2, [30.0, 13.0, 0.0]), "residual only: %s" % y2
+
+
+def pin_i2s_norm_residual_composition():
+    """Random inputs: the fused op equals numpy's RMSNorm (eps = 1e-5) fed to
+    the pinned GEMV, plus the residual; row selection included."""
+    g = np.random.Generator(np.random.PCG64(43))
+    N, K = 11, 512
+    w = g.integers(-1, 2, size=(N, K), dtype=np.int8)
+    x = g.standard_normal(K) * 3.0
+    rw = g.uniform(0.5, 1.5, K)
+    res = g.standard_normal(N)
+    p = O.pack_i2s(w, np.float32(0.625))
+    xn = x / np.sqrt(np.mean(x * x) + 1e-5) * rw
+    ref, _ = O.gemv_i2s(p, xn, N, K)
+    ref = ref + res
+    y, _ = O.gemv_i2s_norm_residual(p, x, N, K, rms_w=rw, eps=1e-5, residual=res)
+    assert np.allclose(y, ref, rtol=1e-12, atol=1e-12), "norm+residual vs composition"
+    rows = np.array([10, 0, 5])
+    y2, _ = O.gemv_i2s_norm_residual(p, x, N, K, rms_w=rw, eps=1e-5, residual=res, rows=rows)
+    assert np.allclose(y2, ref[rows], rtol=1e-12, atol=1e-12), "norm+residual row selection"
+
+
 def pin_i2s_int8_gemm():
     """acc = q W^T exactly (numpy int64 matmul); y = acc * s_act * s_w."""
     g = np.random.Generator(np.random.PCG64(13))

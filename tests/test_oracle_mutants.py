@@ -37,6 +37,10 @@ MUTANTS = {
                                 "int st = orc_gemv_i2s(packed_up, x, N, K, rows, nrows, g, cg);"),
                                ("if (st == ORC_OK) st = orc_gemv_i2s(packed_up, x, N, K, rows, nrows, u, cu);",
                                 "if (st == ORC_OK) st = orc_gemv_i2s(packed_gate, x, N, K, rows, nrows, u, cu);")],
+    "norm_dropped_eps": [("inv = 1.0 / sqrt(ss / (double)K + eps);", "inv = 1.0 / sqrt(ss / (double)K);")],
+    "norm_sum_not_mean": [("inv = 1.0 / sqrt(ss / (double)K + eps);", "inv = 1.0 / sqrt(ss + eps);")],
+    "norm_weight_ignored": [("xn[e] = rms_w ? x[e] * inv * rms_w[e] : x[e];", "xn[e] = rms_w ? x[e] * inv : x[e];")],
+    "residual_dropped": [("y[r] += residual[rows ? rows[r] : r];", "y[r] += 0.0;")],
     "tq2_decode_sign": [("{0, 1, 99, -1}", "{0, -1, 99, 1}")],
     "tq2_shift_order_both_ways": [("return tq2_value_of((blk[j / 4] >> (2 * (j % 4))) & 3);",
                                    "return tq2_value_of((blk[j / 4] >> (6 - 2 * (j % 4))) & 3);"),

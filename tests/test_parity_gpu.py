@@ -243,6 +243,53 @@ def test_gemv_i2s_gate_up_matches_unfused(B):
 
 
 # ---------------------------------------------------------------------------
+# fused residual add, fused RMSNorm + residual
+# ---------------------------------------------------------------------------
+
+def res_gpu(r, yd):
+    return to_gpu(r.astype(np.float32)) if yd == "f32" else bf16_gpu(synth.f32_to_bf16_bits(r.astype(np.float32)))
+
+
+def res_f64(r, yd):
+    return r.astype(np.float32).astype(np.float64) if yd == "f32" else x_f64(synth.f32_to_bf16_bits(r.astype(np.float32)), "bf16")
+
+
+@pytest.mark.parametrize("xd,yd", [("f32", "f32"), ("bf16", "bf16"), ("bf16", "f32")])
+@pytest.mark.parametrize("N,K", [(1, 128), (33, 2560), (257, 6912), (20, 32768)])
+def test_gemv_i2s_residual(B, xd, yd, N, K):
+    g = rng(5 * N + K)
+    w = ternary(g, N, K)
+    x = rand_x(g, K, xd)
+    r = synth.normal_f32(g, (N,)) * 4
+    packed = B.bl_pack_i2s(to_gpu(w), np.float32(1.5))
+    y = B.bl_gemv_i2s_residual(packed, x_gpu(x, xd), res_gpu(r, yd), N, K)
+    yv = y.cpu().numpy().astype(np.float64) if yd == "f32" else x_f64(bits16(y), "bf16")
+    ref, cond = O.gemv_i2s_norm_residual(O.pack_i2s(w, np.float32(1.5)), x_f64(x, xd), N, K, residual=res_f64(r, yd))
+    assert_close(yv, ref, cond, TOL_F32 if yd == "f32" else TOL_BF16, "residual %dx%d" % (N, K))
+
+
+@pytest.mark.parametrize("xd,yd", [("f32", "f32"), ("bf16", "bf16"), ("bf16", "f32")])
+@pytest.mark.parametrize("N,K", [(1, 128), (33, 2560), (2560, 6912), (20, 32768)])
+@pytest.mark.parametrize("with_residual", [True, False])
+def test_gemv_i2s_rmsnorm(B, xd, yd, N, K, with_residual):
+    g = rng(7 * N + K + with_residual)
+    w = ternary(g, N, K)
+    x = rand_x(g, K, xd)
+    rw = (synth.normal_f32(g, (K,)) * 0.1 + 1.0).astype(np.float32)
+    rw_in = rw if xd == "f32" else synth.f32_to_bf16_bits(rw)
+    r = synth.normal_f32(g, (N,)) if with_residual else None
+    packed = B.bl_pack_i2s(to_gpu(w), np.float32(0.75))
+    y = B.bl_gemv_i2s_rmsnorm(packed, x_gpu(x, xd), x_gpu(rw_in, xd), N, K, eps=1e-5,
+                              residual=res_gpu(r, yd) if with_residual else None,
+                              y_dtype=torch.float32 if yd == "f32" else torch.bfloat16)
+    yv = y.cpu().numpy().astype(np.float64) if yd == "f32" else x_f64(bits16(y), "bf16")
+    ref, cond = O.gemv_i2s_norm_residual(O.pack_i2s(w, np.float32(0.75)), x_f64(x, xd), N, K,
+                                         rms_w=x_f64(rw_in, xd), eps=1e-5,
+                                         residual=res_f64(r, yd) if with_residual else None)
+    assert_close(yv, ref, cond, TOL_F32 if yd == "f32" else TOL_BF16, "rmsnorm %dx%d" % (N, K))
+
+
+# ---------------------------------------------------------------------------
 # TQ2_0 GEMV
 # ---------------------------------------------------------------------------
 
@@ -428,6 +475,9 @@ def test_error_paths(B):
     assert e.value.status == B.BL_ERR_ALIGN
     with pytest.raises(B.BLError) as e:
         B.bl_gemv_i2s_gate_up(p, p, x, 4, 96)
+    assert e.value.status == B.BL_ERR_SHAPE
+    with pytest.raises(B.BLError) as e:
+        B.bl_gemv_i2s_rmsnorm(p, x[:1].expand(128).contiguous()[1:], x, 4, 96)
     assert e.value.status == B.BL_ERR_SHAPE
     q = torch.zeros((9, 128), dtype=torch.int8, device="cuda")
     with pytest.raises(B.BLError) as e:
