@@ -416,7 +416,52 @@ def bench_secondary(args, B, torch, stream, dist, hbm, bf16_peak):
         out[wl.name] = {"value": round(tops, 2), "unit": "TOPS (int8 ops)", "frac_bf16_dense_peak": round(tops / bf16_peak, 4),
                         "us_per_launch": t * 1e3}
         del ws
+        out.update(bench_cublas(args, torch, stream, dist, run))
     torch.cuda.synchronize()
+    return out
+
+
+def bench_cublas(args, torch, stream, dist, run):
+    """cuBLAS bf16 (called through torch.matmul) on dense bf16 weights of the same shapes, rotated past L2:
+    the comparison column the binary-gemm card reports its speedups against."""
+    out = {}
+    gen = torch.Generator(device="cuda").manual_seed(1)
+
+    def dense(N, K, copies):
+        return [torch.randn(N, K, device="cuda", dtype=torch.bfloat16, generator=gen) for _ in range(copies)]
+
+    # MLP step, M = 1: gate, up, relu^2 * up, down (3 copies x 106 MB)
+    cps = 3
+    Wg, Wu, Wd = dense(6912, 2560, cps), dense(6912, 2560, cps), dense(2560, 6912, cps)
+    x = torch.randn(1, 2560, device="cuda", dtype=torch.bfloat16, generator=gen)
+
+    def mlp(i):
+        c = i % cps
+        g = torch.matmul(x, Wg[c].t())
+        u = torch.matmul(x, Wu[c].t())
+        h = torch.relu(g) ** 2 * u
+        torch.matmul(h, Wd[c].t())
+
+    t = run(mlp)
+    out["cublas_bf16_mlp_bitnet2b"] = {"us_per_step": t * 1e3, "unit": "us",
+                                       "bf16_weight_GBps": round(3 * 6912 * 2560 * 2 / (t * 1e-3) / 1e9, 1)}
+    del Wg, Wu, Wd
+    # LM head, M = 1, 4, 8 (2 copies x 2.5 GB)
+    W = dense(248320, 5120, 2)
+    for M in (1, 4, 8):
+        xm = torch.randn(M, 5120, device="cuda", dtype=torch.bfloat16, generator=gen)
+        t = run(lambda i: torch.matmul(xm, W[i % 2].t()))
+        out["cublas_bf16_lmhead_248320_M%d" % M] = {"us_per_launch": t * 1e3, "unit": "us",
+                                                    "bf16_weight_GBps": round(248320 * 5120 * 2 / (t * 1e-3) / 1e9, 1)}
+    del W
+    # prefill M = 512 (bf16 GEMM, TFLOP/s)
+    W = dense(6912, 2560, 8)
+    xm = torch.randn(512, 2560, device="cuda", dtype=torch.bfloat16, generator=gen)
+    t = run(lambda i: torch.matmul(xm, W[i % 8].t()))
+    out["cublas_bf16_prefill_512"] = {"us_per_launch": t * 1e3, "unit": "us",
+                                      "tflops": round(2.0 * 512 * 6912 * 2560 / (t * 1e-3) / 1e12, 1)}
+    del W, xm
+    torch.cuda.empty_cache()
     return out
 
 
