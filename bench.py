@@ -402,6 +402,18 @@ def bench_secondary(args, B, torch, stream, dist, hbm, bf16_peak):
             out["%s_M%d" % (wl.name, M)] = {"value": round(gbs, 1), "unit": "GB/s", "frac_hbm": round(gbs / hbm, 4),
                                             "us_per_launch": t * 1e3,
                                             "int_ops_per_s": 2.0 * M * N * K / (t * 1e-3)}
+        # larger batches of the same LM head run on the tensor cores (TOPS)
+        for M in (128, 512):
+            xb = synth.activations(wl.index, M, K, "bf16")
+            q, s = B.bl_quantize_act_absmax_int8(torch.from_numpy(xb.view(np.int16)).cuda().view(torch.bfloat16))
+            y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+            n_l = 40
+            t = dist.max(time_graph(torch, dist, lambda i: B.bl_gemm_w1a8(q, s, wqs[i % 2], wss[i % 2].view(torch.float16),
+                                                                         group=G, y=y), n_l, 4, 4, stream)) / n_l
+            tops = 2.0 * M * N * K / (t * 1e-3) / 1e12
+            out["%s_M%d" % (wl.name, M)] = {"value": round(tops, 1), "unit": "TOPS (int8 ops)",
+                                            "frac_bf16_dense_peak": round(tops / bf16_peak, 4), "us_per_launch": t * 1e3}
+            del y
         del wqs, wss, wq, wsc
 
         # i2_s int8 prefill M = 512 (tensor-bound: TOPS)

@@ -243,7 +243,11 @@ bl_status bl_gemm_w1a8(const int8_t* q, const float* s, const int32_t* wq, const
                        const uint16_t* bias_bf16, int64_t M, int64_t N, int64_t K, int group, uint16_t* y_bf16,
                        int32_t* group_dots, bl_stream_t stream) {
   if (!q || !s || !wq || !ws_fp16 || !y_bf16) return fail(BL_ERR_NULL, "bl_gemm_w1a8: NULL pointer");
-  if (M < 1 || M > 8) return fail(BL_ERR_UNSUPPORTED, "bl_gemm_w1a8: 1 <= M <= 8 supported (M=%lld)", (long long)M);
+  if (M < 1 || M > 0x7fffffff) return fail(BL_ERR_SHAPE, "bl_gemm_w1a8: need M >= 1 (M=%lld)", (long long)M);
+  if (M > 8 && group_dots)
+    return fail(BL_ERR_UNSUPPORTED, "bl_gemm_w1a8: group_dots only for M <= 8 (M=%lld)", (long long)M);
+  if (M > 8 && (K % 128 || K > 132096))
+    return fail(BL_ERR_UNSUPPORTED, "bl_gemm_w1a8: M > 8 needs K %% 128 == 0 and K <= 132096 (K=%lld)", (long long)K);
   if (N < 1 || K < 32 || K % 32 || group < 32 || group % 32 || K % group || N > 0x7fffffff)
     return fail(BL_ERR_SHAPE, "bl_gemm_w1a8: need N >= 1, K %% 32 == 0, group %% 32 == 0, K %% group == 0 "
                 "(N=%lld K=%lld group=%d)", (long long)N, (long long)K, group);

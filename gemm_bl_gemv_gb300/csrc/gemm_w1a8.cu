@@ -215,6 +215,10 @@ cudaError_t dispatch(int M, const int8_t* q, const float* s, const int32_t* wq, 
 cudaError_t launch_gemm_w1a8(const int8_t* q, const float* s, const int32_t* wq, const uint16_t* ws,
                              const uint16_t* bias, int64_t M, int64_t N, int64_t K, int group, uint16_t* y,
                              int32_t* dots, cudaStream_t st) {
+  if (M > 8) {
+    if (dots || !w1a8_tc_applicable(M, K, group)) return cudaErrorNotSupported;
+    return launch_gemm_w1a8_tc(q, s, wq, ws, bias, M, N, K, group, y, st);
+  }
   if (w1a8_rows_applicable(M, K, group)) {
     const cudaError_t e = launch_gemm_w1a8_rows(q, s, wq, ws, bias, M, N, K, group, y, dots, st);
     if (e != cudaErrorNotSupported) return e;

@@ -228,7 +228,7 @@ bl_status bl_gemv_tq2_0(const uint8_t* packed, const void* x, bl_dtype xt, float
                         bl_stream_t stream);
 
 /*
- * W1A8 product for small batches [BG "API" binary_gemm, "Method"]:
+ * W1A8 product [BG "API" binary_gemm, "Method"]:
  *   dot[m,n,g] = sum_{k in group g} w[n,k] q[m,k]              (exact int32)
  *   y[m,n]     = bf16( s[m] * sum_g f32(ws[n,g]) * dot[m,n,g] + bias[n] )
  *   q        : int8 [M, K] activations; s : fp32 [M] per-token scales.
@@ -240,8 +240,11 @@ bl_status bl_gemv_tq2_0(const uint8_t* packed, const void* x, bl_dtype xt, float
  *              dot products are written too (a separate, slower kernel
  *              variant meant for verification).
  * The fp32 sum over groups runs in an order of the library's choosing.
- * Requires 1 <= M <= 8, K % 32 == 0, group % 32 == 0, K % group == 0,
- * N >= 1; wq 16-byte aligned.
+ * M <= 8 runs a CUDA-core kernel (exact int32 group dots, dp4a); M > 8 runs
+ * on the tensor cores with B = +-ws (exact fp16), every product exact and
+ * the sum over K in fp32 (group_dots must then be NULL, and K % 128 == 0).
+ * Requires M >= 1, K % 32 == 0, group % 32 == 0, K % group == 0, N >= 1;
+ * q, wq, ws 16-byte aligned.
  */
 bl_status bl_gemm_w1a8(const int8_t* q, const float* s, const int32_t* wq, const uint16_t* ws_fp16,
                        const uint16_t* bias_bf16, int64_t M, int64_t N, int64_t K, int group, uint16_t* y_bf16,

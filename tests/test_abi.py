@@ -50,7 +50,9 @@ def test_host_checks_without_gpu():
     assert L.bl_gemv_i2s(fake, fake, 7, fake, 0, 4, 128, None) == B.BL_ERR_DTYPE
     assert L.bl_gemv_i2s(ctypes.c_void_p(16 * 1024 + 8), fake, 0, fake, 0, 4, 128, None) == B.BL_ERR_ALIGN
     assert L.bl_gemv_tq2_0(fake, fake, 0, fake, 4, 128, None) == B.BL_ERR_SHAPE
-    assert L.bl_gemm_w1a8(fake, fake, fake, fake, None, 9, 4, 128, 128, fake, None, None) == B.BL_ERR_UNSUPPORTED
+    assert L.bl_gemm_w1a8(fake, fake, fake, fake, None, 9, 4, 128, 128, fake, fake, None) == B.BL_ERR_UNSUPPORTED
+    assert L.bl_gemm_w1a8(fake, fake, fake, fake, None, 9, 4, 96, 32, fake, None, None) == B.BL_ERR_UNSUPPORTED
+    assert L.bl_gemm_w1a8(fake, fake, fake, fake, None, 0, 4, 128, 128, fake, None, None) == B.BL_ERR_SHAPE
     assert L.bl_gemm_w1a8(fake, fake, fake, fake, None, 1, 4, 128, 48, fake, None, None) == B.BL_ERR_SHAPE
     assert L.bl_gemm_i2s_int8(fake, fake, fake, 4, 4, 132224, fake, None, None) == B.BL_ERR_UNSUPPORTED
     assert L.bl_pack_w1(fake, 4, 33, fake, None) == B.BL_ERR_SHAPE

@@ -368,6 +368,25 @@ def test_gemm_w1a8_no_dots_matches_dots_variant(B):
     assert torch.equal(y1.view(torch.int16), y2.view(torch.int16))
 
 
+@pytest.mark.parametrize("M", [9, 64, 130, 512])
+@pytest.mark.parametrize("G", [32, 128, 256])
+@pytest.mark.parametrize("N,K", [(200, 1024), (70, 2560)])
+def test_gemm_w1a8_large_m_tensor_cores(B, M, G, N, K):
+    """M > 8 runs on the tensor cores (B = +-group scale in fp16); with and
+    without bias, against the oracle's fp64 product."""
+    g = rng(M * 31 + G + N + K)
+    w = synth.signs(g, (N, K))
+    xb = synth.f32_to_bf16_bits(synth.normal_f32(g, (M, K)))
+    q, s = B.bl_quantize_act_absmax_int8(bf16_gpu(xb))
+    qo, so = O.quantize_act_absmax_int8(xb, "bf16")
+    ws = synth.abs_normal_fp16_bits(g, (N, K // G), 0.02)
+    bias = synth.f32_to_bf16_bits(synth.normal_f32(g, (N,)) * 0.1) if G == 128 else None
+    y = B.bl_gemm_w1a8(q, s, B.bl_pack_w1(to_gpu(w)), fp16_gpu(ws), bf16_gpu(bias) if bias is not None else None,
+                       group=G)
+    _, yref, cond = O.gemm_w1a8(qo, so, O.pack_w1(w), ws, bias, K, G)
+    assert_close(x_f64(bits16(y), "bf16"), yref, cond, TOL_BF16, "w1a8 tc M=%d G=%d %dx%d" % (M, G, N, K))
+
+
 @pytest.mark.parametrize("M", [1, 4, 8])
 def test_gemm_w1a8_workload_lmhead(B, M):
     """LM head 5120 -> 248320, sampled rows, the benchmark's launch (no dot output)."""
@@ -482,5 +501,5 @@ def test_error_paths(B):
     q = torch.zeros((9, 128), dtype=torch.int8, device="cuda")
     with pytest.raises(B.BLError) as e:
         B.bl_gemm_w1a8(q, torch.ones(9, device="cuda"), torch.zeros((4, 4), dtype=torch.int32, device="cuda"),
-                       torch.zeros((4, 1), dtype=torch.float16, device="cuda"))
+                       torch.zeros((4, 1), dtype=torch.float16, device="cuda"), group_dots=True)
     assert e.value.status == B.BL_ERR_UNSUPPORTED
