@@ -47,7 +47,7 @@ struct Geom {
 };
 
 template <int MT, bool DOTS>
-__global__ void __launch_bounds__(256, (MT <= 4 ? 2 : 1)) gemm_w1a8_rows_kernel(const int8_t* __restrict__ q, const float* __restrict__ s,
+__global__ void __launch_bounds__((MT == 1 ? 512 : 256), (MT >= 2 && MT <= 4 ? 2 : 1)) gemm_w1a8_rows_kernel(const int8_t* __restrict__ q, const float* __restrict__ s,
                                                              const uint8_t* __restrict__ wq,
                                                              const uint8_t* __restrict__ ws,
                                                              const uint16_t* __restrict__ bias,
@@ -288,6 +288,9 @@ __global__ void __launch_bounds__(256, (MT <= 4 ? 2 : 1)) gemm_w1a8_rows_kernel(
 }
 
 bool plan(Geom& g, int M, int64_t N, int64_t K, int G, int max_smem, int nsm) {
+  // up to 16 warps per CTA for one token (more warps hide the decode's
+  // dependency chains; the ring then holds fewer stages per warp), else 8
+  const int max_warps = M == 1 ? 16 : 8;
   auto up = [](uint64_t v, uint64_t a) { return (v + a - 1) / a * a; };
   g.N = int(N);
   g.K = int(K);
@@ -297,9 +300,9 @@ bool plan(Geom& g, int M, int64_t N, int64_t K, int G, int max_smem, int nsm) {
   g.ntiles = int((N + kRows - 1) / kRows);
   const int nu = g.nG / 8;
   int wk = 1;
-  while (wk < 8 && wk < nu && int64_t(g.ntiles) * wk < 8LL * nsm) ++wk;
+  while (wk < 8 && wk < nu && int64_t(g.ntiles) * wk < int64_t(max_warps) * nsm) ++wk;
   g.wk = wk;
-  int wr = std::max(1, 8 / wk);
+  int wr = std::max(1, max_warps / wk);
   while (wr > 1 && (g.ntiles + wr - 1) / wr < nsm) --wr;
   g.wr = wr;
   const int max_units = (nu + wk - 1) / wk;
