@@ -395,13 +395,23 @@ def bench_secondary(args, B, torch, stream, dist, hbm, bf16_peak):
         wbytes = N * K // 8 + N * (K // G) * 2
         for M in (1, 4, 8):
             xb = synth.activations(wl.index, M, K, "bf16")
-            q, s = B.bl_quantize_act_absmax_int8(torch.from_numpy(xb.view(np.int16)).cuda().view(torch.bfloat16))
+            xg = torch.from_numpy(xb.view(np.int16)).cuda().view(torch.bfloat16)
+            q, s = B.bl_quantize_act_absmax_int8(xg)
             y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
             t = run(lambda i: B.bl_gemm_w1a8(q, s, wqs[i % 2], wss[i % 2].view(torch.float16), group=G, y=y))
             gbs = wbytes / (t * 1e-3) / 1e9
+            # from unquantized bf16 x: quantization fused into the product vs the two launches
+            t_f = run(lambda i: B.bl_gemm_w1a8_act(xg, wqs[i % 2], wss[i % 2].view(torch.float16), group=G, y=y))
+
+            def two_calls(i):
+                B.bl_quantize_act_absmax_int8(xg, q, s)
+                B.bl_gemm_w1a8(q, s, wqs[i % 2], wss[i % 2].view(torch.float16), group=G, y=y)
+            t_2 = run(two_calls)
             out["%s_M%d" % (wl.name, M)] = {"value": round(gbs, 1), "unit": "GB/s", "frac_hbm": round(gbs / hbm, 4),
                                             "us_per_launch": t * 1e3,
-                                            "int_ops_per_s": 2.0 * M * N * K / (t * 1e-3)}
+                                            "int_ops_per_s": 2.0 * M * N * K / (t * 1e-3),
+                                            "us_from_bf16_x_fused_quant": t_f * 1e3,
+                                            "us_from_bf16_x_two_launches": t_2 * 1e3}
         # larger batches of the same LM head run on the tensor cores (TOPS)
         for M in (128, 512):
             xb = synth.activations(wl.index, M, K, "bf16")

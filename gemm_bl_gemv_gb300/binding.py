@@ -21,7 +21,7 @@ BL_DEVERR_WAIT_TIMEOUT = 0x1
 EXPORTS = [
     "bl_status_string", "bl_last_error", "bl_device_error", "bl_set_overlap", "bl_get_overlap",
     "bl_pack_i2s", "bl_pack_tq2_0", "bl_pack_w1", "bl_quantize_act_absmax_int8",
-    "bl_gemv_i2s", "bl_gemv_i2s_residual", "bl_gemv_i2s_rmsnorm", "bl_gemv_i2s_gate_up", "bl_gemv_tq2_0", "bl_gemm_w1a8", "bl_gemm_i2s_int8",
+    "bl_gemv_i2s", "bl_gemv_i2s_residual", "bl_gemv_i2s_rmsnorm", "bl_gemv_i2s_gate_up", "bl_gemv_tq2_0", "bl_gemm_w1a8", "bl_gemm_w1a8_act", "bl_gemm_i2s_int8",
 ]
 
 
@@ -49,6 +49,7 @@ def _declare(L):
         "bl_gemv_i2s_rmsnorm": ([p, p, i32, p, ctypes.c_float, p, p, i32, i64, i64, p], st),
         "bl_gemv_tq2_0": ([p, p, i32, p, i64, i64, p], st),
         "bl_gemm_w1a8": ([p, p, p, p, p, i64, i64, i64, i32, p, p, p], st),
+        "bl_gemm_w1a8_act": ([p, i32, p, p, p, i64, i64, i64, i32, p, p], st),
         "bl_gemm_i2s_int8": ([p, p, p, i64, i64, i64, p, p, p], st),
     }
     for name, (args, res) in sig.items():
@@ -252,6 +253,19 @@ def bl_gemm_w1a8(q, s, wq, ws_fp16_bits, bias_bf16_bits=None, group=128, y=None,
     _check(_lib.bl_gemm_w1a8(_ptr(q), _ptr(s), _ptr(wq), _ptr(ws_fp16_bits), _ptr(bias_bf16_bits), M, N, K, group,
                              _ptr(_cuda(y, "y")), _ptr(dots), _stream(stream)))
     return (y, dots) if dots is not None else y
+
+
+def bl_gemm_w1a8_act(x, wq, ws_fp16_bits, bias_bf16_bits=None, group=128, y=None, stream=None):
+    """bl_quantize_act_absmax_int8(x) then bl_gemm_w1a8, in one launch (M <= 8)."""
+    for t, n in ((x, "x"), (wq, "wq"), (ws_fp16_bits, "ws")):
+        _cuda(t, n)
+    M, K = x.shape
+    N = wq.shape[0]
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    _check(_lib.bl_gemm_w1a8_act(_ptr(x), _dtype_code(x), _ptr(wq), _ptr(ws_fp16_bits), _ptr(bias_bf16_bits), M, N, K,
+                                 group, _ptr(_cuda(y, "y")), _stream(stream)))
+    return y
 
 
 def bl_gemm_i2s_int8(q, s, packed, N, y=None, acc=False, stream=None):

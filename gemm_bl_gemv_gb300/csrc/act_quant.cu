@@ -1,12 +1,7 @@
 // Per-token absmax int8 activation quantization ("binary-gemm" card,
-// sections "API" quantize_activation and "Correctness").  The card states
-// per-token absmax with under 1% reconstruction error; the formula below is
-// this library's reading, computed in binary32 with round-to-nearest-even:
-//   amax = max_k |x[m,k]|;  amax == 0 -> q = 0, s = 0;
-//   inv  = 127 / amax;  q = clamp(rint(x * inv), -127, 127);  s = amax / 127.
-// Division and multiplication use the _rn intrinsics so that no fused or
-// approximate operation changes a rounding.
-#include "bl_device.cuh"
+// sections "API" quantize_activation and "Correctness"), one CTA per token;
+// the formula and its binary32 steps are in act_quant.cuh.
+#include "act_quant.cuh"
 #include "bl_internal.h"
 
 namespace bl {
@@ -36,15 +31,15 @@ __global__ void __launch_bounds__(256) act_quant_kernel(const void* __restrict__
   if (tid == 0) {
     float amax = 0.f;
     for (int w = 0; w < int(blockDim.x / 32); ++w) amax = fmaxf(amax, red[w]);
-    s_inv = amax == 0.f ? 0.f : __fdiv_rn(127.0f, amax);
-    s[m] = amax == 0.f ? 0.f : __fdiv_rn(amax, 127.0f);
+    float sc, iv;
+    absmax_scales(amax, sc, iv);
+    s_inv = iv;
+    s[m] = sc;
   }
   __syncthreads();
   const float inv = s_inv;
   for (int64_t k = tid; k < K; k += blockDim.x) {
-    float r = rintf(__fmul_rn(load<XB>(x, base + k), inv));
-    r = fminf(fmaxf(r, -127.f), 127.f);
-    q[base + k] = int8_t(int(r));
+    q[base + k] = int8_t(quant_code(load<XB>(x, base + k), inv));
   }
   pdl_launch_dependents();
 }

@@ -259,6 +259,25 @@ bl_status bl_gemm_w1a8(const int8_t* q, const float* s, const int32_t* wq, const
                      "bl_gemm_w1a8");
 }
 
+bl_status bl_gemm_w1a8_act(const void* x, bl_dtype xt, const int32_t* wq, const uint16_t* ws_fp16,
+                           const uint16_t* bias_bf16, int64_t M, int64_t N, int64_t K, int group, uint16_t* y_bf16,
+                           bl_stream_t stream) {
+  if (!x || !wq || !ws_fp16 || !y_bf16) return fail(BL_ERR_NULL, "bl_gemm_w1a8_act: NULL pointer");
+  if (xt != BL_F32 && xt != BL_BF16) return fail(BL_ERR_DTYPE, "bl_gemm_w1a8_act: bad dtype %d", int(xt));
+  if (N < 1 || K < 32 || K % 32 || group < 32 || group % 32 || K % group || N > 0x7fffffff || M < 1)
+    return fail(BL_ERR_SHAPE, "bl_gemm_w1a8_act: need M, N >= 1, K %% 32 == 0, group %% 32 == 0, K %% group == 0 "
+                "(M=%lld N=%lld K=%lld group=%d)", (long long)M, (long long)N, (long long)K, group);
+  if (M > 8)
+    return fail(BL_ERR_UNSUPPORTED, "bl_gemm_w1a8_act: M <= 8 only; quantize larger batches with "
+                "bl_quantize_act_absmax_int8 (M=%lld)", (long long)M);
+  if (K / group > 1024) return fail(BL_ERR_UNSUPPORTED, "bl_gemm_w1a8_act: at most 1024 groups per row");
+  if (!aligned(x, 16) || !aligned(wq, 16) || !aligned(ws_fp16, 16) || !aligned(y_bf16, 2) ||
+      (bias_bf16 && !aligned(bias_bf16, 2)))
+    return fail(BL_ERR_ALIGN, "bl_gemm_w1a8_act: x, wq, ws must be 16-byte aligned; y, bias 2-byte aligned");
+  return cuda_status(launch_gemm_w1a8_act(x, xt, wq, ws_fp16, bias_bf16, M, N, K, group, y_bf16, S(stream)),
+                     "bl_gemm_w1a8_act");
+}
+
 bl_status bl_gemm_i2s_int8(const int8_t* q, const float* s, const uint8_t* packed, int64_t M, int64_t N, int64_t K,
                            float* y, int32_t* acc, bl_stream_t stream) {
   if (!q || !s || !packed || !y) return fail(BL_ERR_NULL, "bl_gemm_i2s_int8: NULL pointer");

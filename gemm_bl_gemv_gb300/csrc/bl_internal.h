@@ -102,6 +102,14 @@ cudaError_t launch_gemm_w1a8_tc(const int8_t* q, const float* s, const int32_t* 
 cudaError_t launch_gemm_w1a8_rows(const int8_t* q, const float* s, const int32_t* wq, const uint16_t* ws,
                                   const uint16_t* bias, int64_t M, int64_t N, int64_t K, int group, uint16_t* y,
                                   int32_t* dots, cudaStream_t st);
+// W1A8 with the per-token act quantization fused in (M <= 8): the
+// lane-per-row kernel where it applies, else the tiled kernel.
+cudaError_t launch_gemm_w1a8_act(const void* x, bl_dtype xt, const int32_t* wq, const uint16_t* ws,
+                                 const uint16_t* bias, int64_t M, int64_t N, int64_t K, int group, uint16_t* y,
+                                 cudaStream_t st);
+cudaError_t launch_gemm_w1a8_act_tiled(const void* x, bl_dtype xt, const int32_t* wq, const uint16_t* ws,
+                                       const uint16_t* bias, int64_t M, int64_t N, int64_t K, int group, uint16_t* y,
+                                       cudaStream_t st);
 cudaError_t launch_gemm_i2s_int8_simt(const int8_t* q, const float* sc, const uint8_t* packed, int64_t M, int64_t N,
                                       int64_t K, float* y, int32_t* acc, cudaStream_t s);
 cudaError_t launch_gemm_i2s_int8(const int8_t* q, const float* sc, const uint8_t* packed, int64_t M, int64_t N,

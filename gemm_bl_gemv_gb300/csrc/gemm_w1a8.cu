@@ -1,5 +1,5 @@
 // W1A8 product for 1 <= M <= 8 tokens, tiled kernel for shapes the
-// lane-per-row kernel (gemm_w1a8_rows.cu) does not take ("binary-gemm"
+// lane-per-row kernel (gemm_w1a8_rows.cuh) does not take ("binary-gemm"
 // card, sections "API" binary_gemm and "Method"):
 //   dot[m,n,g] = sum_{k in g} w[n,k] q[m,k]     (exact)
 //   y[m,n]     = bf16( s[m] * sum_g ws[n,g] * dot[m,n,g] + bias[n] )
@@ -16,6 +16,11 @@
 //
 // A chunk of the tiled skeleton is one scale group (group/32 words); the
 // group scales of the tile's rows travel in the same bulk copy as the bits.
+//
+// XQ != 0: the kernel takes unquantized activations (1 = fp32, 2 = bf16) and
+// quantizes them per token in its prologue with the helpers of act_quant.cuh,
+// so the codes and scales are those of the stand-alone kernel.
+#include "act_quant.cuh"
 #include "bl_internal.h"
 #include "gemv_tiled.cuh"
 
@@ -24,12 +29,13 @@ namespace {
 
 constexpr int kW1R = 4;
 
-template <int MT, bool DOTS>
+template <int MT, bool DOTS, int XQ>
 struct W1a8Policy {
   static constexpr int kMaxThreads = 1024;
   struct Args {
     const int8_t* q;
     const float* s;
+    const void* x;  // XQ != 0: [MT, K] activations to quantize
     const int32_t* wq;
     const uint16_t* ws;
     const uint16_t* bias;
@@ -37,9 +43,13 @@ struct W1a8Policy {
     int32_t* dots;
     int N, K, G;
   };
-  // policy area: [qd: MT x WPC x 8 x nC u32][qsum: MT x nC int]
+  // policy area: [qd: MT x WPC x 8 x nC u32][qsum: MT x nC int][8 spare]
+  //              [XQ: reduction 32 x MT, scale MT, inv MT floats]
   static __host__ __device__ uint32_t qd_words(int nC, int wpc) { return uint32_t(MT) * wpc * 8u * nC; }
-  static __host__ __device__ uint32_t bytes(int nC, int wpc) { return (qd_words(nC, wpc) + MT * nC + 8) * 4; }
+  static __host__ __device__ uint32_t tq_word(int nC, int wpc) { return qd_words(nC, wpc) + MT * nC + 8; }
+  static __host__ __device__ uint32_t bytes(int nC, int wpc) {
+    return (tq_word(nC, wpc) + (XQ ? 34 * MT : 0)) * 4;
+  }
 
   static __device__ const uint8_t* weights(const Args& a) { return reinterpret_cast<const uint8_t*>(a.wq); }
   static __device__ const uint8_t* aux(const Args& a) { return reinterpret_cast<const uint8_t*>(a.ws); }
@@ -52,15 +62,30 @@ struct W1a8Policy {
     uint32_t* qd = reinterpret_cast<uint32_t*>(smem + g.off_pol);
     const int nC = g.nC, wpc = a.G / 32;
     int* qsum = reinterpret_cast<int*>(qd + qd_words(nC, wpc));
+    float* tq = reinterpret_cast<float*>(qd + tq_word(nC, wpc));
+    if (XQ) token_scales<MT, XQ == 2>(a.x, a.K, tq, tq + 32 * MT, tq + 33 * MT);
     // one (token m, group c, word w) per iteration: elements G*c + 32w + 0..31
     for (int idx = tid; idx < MT * nC * wpc; idx += T) {
       const int m = idx / (nC * wpc);
       const int c = (idx / wpc) % nC;
       const int w = idx % wpc;
-      const uint32_t* src = reinterpret_cast<const uint32_t*>(a.q + int64_t(m) * a.K + int64_t(a.G) * c + 32 * w);
+      const int64_t e0 = int64_t(m) * a.K + int64_t(a.G) * c + 32 * w;
       uint32_t v[8];
+      if (XQ) {
+        const float inv = tq[33 * MT + m];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) v[k] = src[k];
+        for (int k = 0; k < 4; ++k) {
+          float f[8];
+          load8<XQ == 2>(a.x, e0 / 8 + k, f);
+          const uint2 b = quant8(f, inv);
+          v[2 * k] = b.x;
+          v[2 * k + 1] = b.y;
+        }
+      } else {
+        const uint32_t* src = reinterpret_cast<const uint32_t*>(a.q + e0);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) v[k] = src[k];
+      }
       const int step = (w - rot(c, wpc) + wpc) % wpc;
       // class j collects bytes j, j+8, j+16, j+24 of the 32 activation bytes
 #pragma unroll
@@ -151,17 +176,20 @@ struct W1a8Policy {
       const float* pr = part + (m * g.TR + r) * g.nC;
       float acc = 0.f;
       for (int c = 0; c < g.nC; ++c) acc += pr[c];
-      float yv = acc * a.s[m];
+      const float sm = XQ ? reinterpret_cast<const float*>(
+                                reinterpret_cast<const uint32_t*>(smem + g.off_pol) + tq_word(g.nC, a.G / 32))[32 * MT + m]
+                          : a.s[m];
+      float yv = acc * sm;
       if (a.bias) yv += bf16_bits_to_f32(a.bias[row0 + r]);
       a.y[int64_t(m) * a.N + row0 + r] = f32_to_bf16_bits_rn(yv);
     }
   }
 };
 
-template <int MT, bool DOTS>
-cudaError_t run(const int8_t* q, const float* s, const int32_t* wq, const uint16_t* ws, const uint16_t* bias,
-                int64_t N, int64_t K, int G, uint16_t* y, int32_t* dots, cudaStream_t st) {
-  using Pol = W1a8Policy<MT, DOTS>;
+template <int MT, bool DOTS, int XQ>
+cudaError_t run(const int8_t* q, const float* s, const void* x, const int32_t* wq, const uint16_t* ws,
+                const uint16_t* bias, int64_t N, int64_t K, int G, uint16_t* y, int32_t* dots, cudaStream_t st) {
+  using Pol = W1a8Policy<MT, DOTS, XQ>;
   const int nC = int(K / G), wpc = G / 32;
   int P = 256 / nC;
   if (P < 1) P = 1;
@@ -189,23 +217,23 @@ cudaError_t run(const int8_t* q, const float* s, const int32_t* wq, const uint16
   if (blocks_per_sm < 1) blocks_per_sm = 1;
   int grid = sm_count() * blocks_per_sm;
   if (grid > g.ntiles) grid = g.ntiles;
-  typename Pol::Args a{q, s, wq, ws, bias, y, dots, int(N), int(K), G};
+  typename Pol::Args a{q, s, x, wq, ws, bias, y, dots, int(N), int(K), G};
   const bool pdl = overlap_enabled();
   return launch(kern, dim3(grid), dim3(threads), g.smem_bytes, st, pdl, a, g, pdl ? 1 : 0);
 }
 
-template <bool DOTS>
-cudaError_t dispatch(int M, const int8_t* q, const float* s, const int32_t* wq, const uint16_t* ws,
+template <bool DOTS, int XQ>
+cudaError_t dispatch(int M, const int8_t* q, const float* s, const void* x, const int32_t* wq, const uint16_t* ws,
                      const uint16_t* bias, int64_t N, int64_t K, int G, uint16_t* y, int32_t* dots, cudaStream_t st) {
   switch (M) {
-    case 1: return run<1, DOTS>(q, s, wq, ws, bias, N, K, G, y, dots, st);
-    case 2: return run<2, DOTS>(q, s, wq, ws, bias, N, K, G, y, dots, st);
-    case 3: return run<3, DOTS>(q, s, wq, ws, bias, N, K, G, y, dots, st);
-    case 4: return run<4, DOTS>(q, s, wq, ws, bias, N, K, G, y, dots, st);
-    case 5: return run<5, DOTS>(q, s, wq, ws, bias, N, K, G, y, dots, st);
-    case 6: return run<6, DOTS>(q, s, wq, ws, bias, N, K, G, y, dots, st);
-    case 7: return run<7, DOTS>(q, s, wq, ws, bias, N, K, G, y, dots, st);
-    case 8: return run<8, DOTS>(q, s, wq, ws, bias, N, K, G, y, dots, st);
+    case 1: return run<1, DOTS, XQ>(q, s, x, wq, ws, bias, N, K, G, y, dots, st);
+    case 2: return run<2, DOTS, XQ>(q, s, x, wq, ws, bias, N, K, G, y, dots, st);
+    case 3: return run<3, DOTS, XQ>(q, s, x, wq, ws, bias, N, K, G, y, dots, st);
+    case 4: return run<4, DOTS, XQ>(q, s, x, wq, ws, bias, N, K, G, y, dots, st);
+    case 5: return run<5, DOTS, XQ>(q, s, x, wq, ws, bias, N, K, G, y, dots, st);
+    case 6: return run<6, DOTS, XQ>(q, s, x, wq, ws, bias, N, K, G, y, dots, st);
+    case 7: return run<7, DOTS, XQ>(q, s, x, wq, ws, bias, N, K, G, y, dots, st);
+    case 8: return run<8, DOTS, XQ>(q, s, x, wq, ws, bias, N, K, G, y, dots, st);
   }
   return cudaErrorInvalidValue;
 }
@@ -223,8 +251,15 @@ cudaError_t launch_gemm_w1a8(const int8_t* q, const float* s, const int32_t* wq,
     const cudaError_t e = launch_gemm_w1a8_rows(q, s, wq, ws, bias, M, N, K, group, y, dots, st);
     if (e != cudaErrorNotSupported) return e;
   }
-  if (dots) return dispatch<true>(int(M), q, s, wq, ws, bias, N, K, group, y, dots, st);
-  return dispatch<false>(int(M), q, s, wq, ws, bias, N, K, group, y, dots, st);
+  if (dots) return dispatch<true, 0>(int(M), q, s, nullptr, wq, ws, bias, N, K, group, y, dots, st);
+  return dispatch<false, 0>(int(M), q, s, nullptr, wq, ws, bias, N, K, group, y, dots, st);
+}
+
+cudaError_t launch_gemm_w1a8_act_tiled(const void* x, bl_dtype xt, const int32_t* wq, const uint16_t* ws,
+                                       const uint16_t* bias, int64_t M, int64_t N, int64_t K, int group, uint16_t* y,
+                                       cudaStream_t st) {
+  if (xt == BL_BF16) return dispatch<false, 2>(int(M), nullptr, nullptr, x, wq, ws, bias, N, K, group, y, nullptr, st);
+  return dispatch<false, 1>(int(M), nullptr, nullptr, x, wq, ws, bias, N, K, group, y, nullptr, st);
 }
 
 }  // namespace bl

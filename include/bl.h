@@ -251,6 +251,22 @@ bl_status bl_gemm_w1a8(const int8_t* q, const float* s, const int32_t* wq, const
                        int32_t* group_dots, bl_stream_t stream);
 
 /*
+ * W1A8 product with the activation quantization fused in
+ * [BG "API" quantize_activation and binary_gemm, "Method"]:
+ *   the same y as bl_quantize_act_absmax_int8(x) followed by bl_gemm_w1a8,
+ *   bit for bit, in one launch: every CTA quantizes the M tokens itself.
+ *   x : [M, K] fp32 or bf16 (xt), unquantized activations.
+ *   wq, ws_fp16, bias_bf16, y_bf16 : as for bl_gemm_w1a8.
+ * Decode sizes only: 1 <= M <= 8 (BL_ERR_UNSUPPORTED above; larger batches
+ * take the two calls).  Otherwise the requirements of bl_gemm_w1a8 for
+ * M <= 8: K % 32 == 0, group % 32 == 0, K % group == 0, at most 1024 groups
+ * per row.  x, wq, ws 16-byte aligned.
+ */
+bl_status bl_gemm_w1a8_act(const void* x, bl_dtype xt, const int32_t* wq, const uint16_t* ws_fp16,
+                           const uint16_t* bias_bf16, int64_t M, int64_t N, int64_t K, int group, uint16_t* y_bf16,
+                           bl_stream_t stream);
+
+/*
  * i2_s product with int8 activations (prefill, large M)
  * [BL "BitLinear Mathematics"; activations as BG "quantize_activation"]:
  *   acc[m,n] = sum_k q[m,k] w[n,k]          (exact int32)

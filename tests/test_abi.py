@@ -55,6 +55,14 @@ def test_host_checks_without_gpu():
     assert L.bl_gemm_w1a8(fake, fake, fake, fake, None, 0, 4, 128, 128, fake, None, None) == B.BL_ERR_SHAPE
     assert L.bl_gemm_w1a8(fake, fake, fake, fake, None, 1, 4, 128, 48, fake, None, None) == B.BL_ERR_SHAPE
     assert L.bl_gemm_i2s_int8(fake, fake, fake, 4, 4, 132224, fake, None, None) == B.BL_ERR_UNSUPPORTED
+    assert L.bl_gemm_w1a8_act(fake, 1, fake, fake, None, 9, 4, 1024, 128, fake, None) == B.BL_ERR_UNSUPPORTED
+    assert L.bl_gemm_w1a8_act(fake, 1, fake, fake, None, 1, 4, 65536, 32, fake, None) == B.BL_ERR_UNSUPPORTED
+    assert L.bl_gemm_w1a8_act(fake, 1, fake, fake, None, 1, 4, 1024, 48, fake, None) == B.BL_ERR_SHAPE
+    assert L.bl_gemm_w1a8_act(fake, 5, fake, fake, None, 1, 4, 1024, 128, fake, None) == B.BL_ERR_DTYPE
+    assert L.bl_gemm_w1a8_act(fake, 1, fake, fake, None, 0, 4, 1024, 128, fake, None) == B.BL_ERR_SHAPE
+    assert L.bl_gemm_w1a8_act(None, 1, fake, fake, None, 1, 4, 1024, 128, fake, None) == B.BL_ERR_NULL
+    assert L.bl_gemm_w1a8_act(ctypes.c_void_p(16 * 1024 + 4), 0, fake, fake, None, 1, 4, 1024, 128, fake,
+                              None) == B.BL_ERR_ALIGN
     assert L.bl_pack_w1(fake, 4, 33, fake, None) == B.BL_ERR_SHAPE
     assert L.bl_quantize_act_absmax_int8(fake, 3, 1, 8, fake, fake, None) == B.BL_ERR_DTYPE
     assert b"K % 128" in L.bl_last_error() or b"bl_" in L.bl_last_error()

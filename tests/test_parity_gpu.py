@@ -408,6 +408,58 @@ def test_gemm_w1a8_workload_lmhead(B, M):
     assert_close(x_f64(yb[:, rows], "bf16"), yref, cond, TOL_BF16, "lm head M=%d" % M)
 
 
+@pytest.mark.parametrize("xdt", ["bf16", "f32"])
+@pytest.mark.parametrize("M", [1, 2, 5, 8])
+@pytest.mark.parametrize("G,N,K", [(32, 37, 256), (128, 100, 1024), (256, 300, 4096), (128, 129, 2560),
+                                   (64, 45, 1280), (32, 20, 96)])
+def test_gemm_w1a8_act_fused(B, xdt, M, G, N, K):
+    """Act quantization fused into the W1A8 prologue: the same bits as the two
+    calls, and the oracle's quantization followed by its product.  The first
+    three shapes take the lane-per-row kernel, the others the tiled one."""
+    g = rng(M * 7 + G + N + K + (xdt == "f32"))
+    w = synth.signs(g, (N, K))
+    x = synth.normal_f32(g, (M, K))
+    if M > 1:
+        x[1, :] = 0  # an all-zero token: s = 0 and q = 0
+    if M > 2:
+        x[2, 5] = -1000.0  # one outlier sets the token's absmax
+    if xdt == "bf16":
+        x = synth.f32_to_bf16_bits(x)
+    ws = synth.abs_normal_fp16_bits(g, (N, K // G), 0.02)
+    bias = synth.f32_to_bf16_bits(synth.normal_f32(g, (N,))) if M % 2 else None
+    wq = B.bl_pack_w1(to_gpu(w))
+    biasg = None if bias is None else bf16_gpu(bias)
+    xg = x_gpu(x, xdt)
+    y = B.bl_gemm_w1a8_act(xg, wq, fp16_gpu(ws), biasg, group=G)
+    q, s = B.bl_quantize_act_absmax_int8(xg)
+    y2 = B.bl_gemm_w1a8(q, s, wq, fp16_gpu(ws), biasg, group=G)
+    assert torch.equal(y.view(torch.int16), y2.view(torch.int16)), "fused must equal the two-call sequence"
+    qo, so = O.quantize_act_absmax_int8(x, xdt)
+    _, yref, cond = O.gemm_w1a8(qo, so, O.pack_w1(w), ws, bias, K, G)
+    assert_close(x_f64(bits16(y), "bf16"), yref, cond, TOL_BF16, "w1a8 act M=%d G=%d %dx%d" % (M, G, N, K))
+
+
+@pytest.mark.parametrize("M", [1, 8])
+def test_gemm_w1a8_act_workload_lmhead(B, M):
+    """LM head 5120 -> 248320 with fused quantization, sampled rows."""
+    wl = synth.WORKLOADS["w1a8_lmhead_248320"]
+    N, K, G = wl.N, wl.K, wl.group
+    wq = torch.empty((N, K // 32), dtype=torch.int32, device="cuda")
+    for b in range((N + synth.ROW_BLOCK - 1) // synth.ROW_BLOCK):
+        blk = synth.weight_block(wl.index, "w", N, K, b, "signs")
+        r0 = b * synth.ROW_BLOCK
+        B.bl_pack_w1(to_gpu(blk), out=wq[r0:r0 + blk.shape[0]])
+    ws = synth.block_scale_matrix(wl.index, N, K // G, tensor="group_scale")
+    xb = synth.activations(wl.index, M, K, "bf16")
+    y = B.bl_gemm_w1a8_act(bf16_gpu(xb), wq, fp16_gpu(ws), group=G)
+    yb = bits16(y)
+    q, s = O.quantize_act_absmax_int8(xb, "bf16")
+    rows = np.unique(np.concatenate([[0, 1, N - 1, N - 2], rng(M + 5).integers(0, N, 60)]))
+    wrows = synth.weight_rows(wl.index, "w", N, K, rows, "signs")
+    _, yref, cond = O.gemm_w1a8(q, s, O.pack_w1(wrows), ws[rows], None, K, G)
+    assert_close(x_f64(yb[:, rows], "bf16"), yref, cond, TOL_BF16, "lm head act M=%d" % M)
+
+
 # ---------------------------------------------------------------------------
 # i2_s x int8 (prefill)
 # ---------------------------------------------------------------------------
