@@ -444,6 +444,51 @@ int orc_gemv_tq2_0(const uint8_t* packed, const double* x, int64_t N, int64_t K,
   return bad ? (bad & 1 ? ORC_ERR_SHAPE : ORC_ERR_VALUE) : ORC_OK;
 }
 
+/*
+ * TQ2_0 weights against int8 activations (large batches).  The TQ2_0 page
+ * defines the container and the per-block value d_b * w; the activations
+ * are the per-token int8 codes and fp32 scales of the "binary-gemm" card's
+ * quantize_activation.  Reading: the product is the definition with x
+ * replaced by its quantized form s_m * q[m,:]:
+ *   dot[m,n,b] = sum_{j<256} w[n,256b+j] q[m,256b+j]          (exact int64)
+ *   y[m,r]     = s_m * sum_b d[n,b] * dot[m,n,b]               (fp64)
+ *   cond[m,r]  = |s_m| * sum_b |d[n,b]| * sum_j |w| |q|.
+ */
+int orc_gemm_tq2_0_int8(const int8_t* q, const float* s_act, const uint8_t* packed,
+                        int64_t M, int64_t N, int64_t K, const int64_t* rows, int64_t nrows,
+                        double* y, double* cond) {
+  if (M < 0 || N < 0 || K < 0 || K % 256 != 0) return ORC_ERR_SHAPE;
+  const int64_t nb = K / 256;
+  int bad = 0;
+#ifdef _OPENMP
+#pragma omp parallel for num_threads(g_threads) schedule(static) reduction(| : bad)
+#endif
+  for (int64_t r = 0; r < nrows; ++r) {
+    const int64_t n = rows ? rows[r] : r;
+    if (n < 0 || n >= N) { bad |= 1; continue; }
+    for (int64_t m = 0; m < M; ++m) {
+      double total = 0.0, c = 0.0;
+      for (int64_t b = 0; b < nb; ++b) {
+        const double d = orc_fp16_to_double(tq2_scale_bits(packed, K, n, b));
+        int64_t dot = 0, dot_abs = 0;
+        for (int64_t j = 0; j < 256; ++j) {
+          const int64_t e = b * 256 + j;
+          const int w = tq2_weight(packed, K, n, e);
+          if (w == 99) { bad |= 2; break; }
+          dot += (int64_t)q[m * K + e] * w;
+          dot_abs += (int64_t)abs(q[m * K + e]) * abs(w);
+        }
+        total += d * (double)dot;
+        c += fabs(d) * (double)dot_abs;
+      }
+      const double sm = (double)s_act[m];
+      y[m * nrows + r] = sm * total;
+      if (cond) cond[m * nrows + r] = fabs(sm) * c;
+    }
+  }
+  return bad ? (bad & 1 ? ORC_ERR_SHAPE : ORC_ERR_VALUE) : ORC_OK;
+}
+
 /* ------------------------------------------------------------------ */
 /* W1 sign bits ("binary-gemm": API, Method, Correctness)              */
 /*   {-1,+1} int8 [N,K] -> int32 [N,K/32], stored bit b = (w+1)/2;     */

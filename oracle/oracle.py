@@ -42,6 +42,7 @@ def load(path):
         "orc_pack_tq2_0": ([p, p, i64, i64, p], ctypes.c_int),
         "orc_unpack_tq2_0": ([p, i64, i64, p, p], ctypes.c_int),
         "orc_gemv_tq2_0": ([p, p, i64, i64, p, i64, p, p], ctypes.c_int),
+        "orc_gemm_tq2_0_int8": ([p, p, p, i64, i64, i64, p, i64, p, p], ctypes.c_int),
         "orc_pack_w1": ([p, i64, i64, p], ctypes.c_int),
         "orc_unpack_w1": ([p, i64, i64, p], ctypes.c_int),
         "orc_gemm_w1a8": ([p, p, p, p, p, i64, i64, i64, i64, p, i64, p, p, p], ctypes.c_int),
@@ -213,6 +214,20 @@ def gemv_tq2_0(packed, x, N, K, rows=None):
     y = np.empty(nr, np.float64)
     c = np.empty(nr, np.float64)
     _check(lib().orc_gemv_tq2_0(_ptr(p), _ptr(x), N, K, _ptr(r), nr, _ptr(y), _ptr(c)), "gemv_tq2_0")
+    return y, c
+
+
+def gemm_tq2_0_int8(q, s_act, packed, N, K, rows=None):
+    """y[m, r] = s_m * sum_b d[n,b] * (exact block dot of w and q); returns (y, cond), [M, nrows]."""
+    q = _c(q, np.int8)
+    M = q.shape[0]
+    s = _c(s_act, np.float32)
+    p = _c(packed, np.uint8)
+    r, nr = _rows(rows, N)
+    y = np.empty((M, nr), np.float64)
+    c = np.empty((M, nr), np.float64)
+    _check(lib().orc_gemm_tq2_0_int8(_ptr(q), _ptr(s), _ptr(p), M, N, K, _ptr(r), nr, _ptr(y), _ptr(c)),
+           "gemm_tq2_0_int8")
     return y, c
 
 

@@ -329,6 +329,40 @@ def pin_tq2_0_gemv():
     assert np.allclose(yneg, -256.0 * dd.sum(1), rtol=1e-14), "tq2_0 closed form (-1)"
 
 
+def pin_tq2_0_int8_gemm():
+    """y = s_m * sum_b d_b * (q_b W_b^T) with the block dots from numpy int64
+    matmul and d decoded by numpy float16; the closed form y = 256 s sum_b d_b
+    for W = +1, q = 1; and, with one scale for every block, the i2_s int8
+    product of the same ternary matrix with that scale as its tensor scale."""
+    g = np.random.Generator(np.random.PCG64(19))
+    M, N, K = 5, 7, 768
+    w = g.integers(-1, 2, size=(N, K), dtype=np.int8)
+    q = g.integers(-127, 128, size=(M, K), dtype=np.int8)
+    sa = g.uniform(0.01, 0.1, M).astype(np.float32)
+    d = (np.abs(g.standard_normal((N, K // 256))) * 0.02).astype(np.float16).view(np.uint16)
+    d[0, 1] = 0x8000 | d[0, 1]  # a negative block scale
+    y, cond = O.gemm_tq2_0_int8(q, sa, O.pack_tq2_0(w, d), N, K)
+    dd = fp16_np(d)
+    dots = [q[:, 256 * b:256 * (b + 1)].astype(np.int64) @ w[:, 256 * b:256 * (b + 1)].astype(np.int64).T
+            for b in range(K // 256)]
+    ref = sum(dd[None, :, b] * dots[b] for b in range(K // 256)) * sa[:, None].astype(np.float64)
+    assert np.allclose(y, ref, rtol=1e-13, atol=1e-300), "tq2_0 int8 vs blockwise int matmul"
+    dabs = [np.abs(q[:, 256 * b:256 * (b + 1)]).astype(np.int64) @ np.abs(w[:, 256 * b:256 * (b + 1)]).T
+            for b in range(K // 256)]
+    refc = sum(np.abs(dd[None, :, b]) * dabs[b] for b in range(K // 256)) * sa[:, None]
+    assert np.allclose(cond, refc, rtol=1e-12), "tq2_0 int8 cond"
+    rows = np.array([6, 0])
+    y2, _ = O.gemm_tq2_0_int8(q, sa, O.pack_tq2_0(w, d), N, K, rows=rows)
+    assert np.array_equal(y2, y[:, rows])
+    ones = np.ones((N, K), np.int8)
+    y1, _ = O.gemm_tq2_0_int8(np.ones((1, K), np.int8), np.ones(1, np.float32), O.pack_tq2_0(ones, d), N, K)
+    assert np.allclose(y1[0], 256.0 * dd.sum(1), rtol=1e-14), "tq2_0 int8 closed form"
+    one_scale = np.full((N, K // 256), 0x3A00, np.uint16)  # 0.75 in every block
+    yt, _ = O.gemm_tq2_0_int8(q, sa, O.pack_tq2_0(w, one_scale), N, K)
+    _, yi, _ = O.gemm_i2s_int8(q, sa, O.pack_i2s(w, np.float32(0.75)), N, K)
+    assert np.allclose(yt, yi, rtol=1e-14, atol=0), "tq2_0 int8 with one scale = i2_s int8"
+
+
 def pin_w1_golden_words():
     for name, w, words in golden_w1():
         got = O.pack_w1(w)

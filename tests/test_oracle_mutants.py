@@ -50,6 +50,10 @@ MUTANTS = {
     "tq2_dropped_block_scale": [("total += d * blk;", "total += blk;")],
     "tq2_block_stride_both_ways": [("return packed + (n * (K / 256) + b) * 66;", "return packed + (n * (K / 256) + b) * 64;"),
                                    ("uint8_t* blk = out + (n * nb + b) * 66;", "uint8_t* blk = out + (n * nb + b) * 64;")],
+    "tq2_int8_dropped_block_scale": [("total += d * (double)dot;", "total += (double)dot;")],
+    "tq2_int8_dropped_token_scale": [("y[m * nrows + r] = sm * total;", "y[m * nrows + r] = total;")],
+    "tq2_int8_q_transposed": [("dot += (int64_t)q[m * K + e] * w;", "dot += (int64_t)q[e * M + m] * w;")],
+    "tq2_int8_q_block_shift": [("dot += (int64_t)q[m * K + e] * w;", "dot += (int64_t)q[m * K + (e + 1) % K] * w;")],
     "w1_bit_order_both_ways": [("word |= bit << i;", "word |= bit << (31 - i);"),
                                ("return ((word >> (k % 32)) & 1u) ? 1 : -1;", "return ((word >> (31 - k % 32)) & 1u) ? 1 : -1;")],
     "w1_zero_as_plus": [("const uint32_t bit = (v == 1) ? 1u : 0u;", "const uint32_t bit = (v >= 0) ? 1u : 0u;")],
