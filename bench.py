@@ -381,7 +381,16 @@ def bench_secondary(args, B, torch, stream, dist, hbm, bf16_peak):
         nbytes = wl.N * (wl.K // 256) * 66
         gbs = nbytes / (t * 1e-3) / 1e9
         out[wl.name] = {"value": round(gbs, 1), "unit": "GB/s", "frac_hbm": round(gbs / hbm, 4), "us_per_launch": t * 1e3}
-        del ws, p0
+        # the same TQ2_0 weights against 512 int8 tokens (tensor cores: TOPS)
+        Mq = 512
+        xb = synth.activations(wl.index, Mq, wl.K, "bf16")
+        q, s = B.bl_quantize_act_absmax_int8(torch.from_numpy(xb.view(np.int16)).cuda().view(torch.bfloat16))
+        y = torch.empty((Mq, wl.N), dtype=torch.float32, device="cuda")
+        t = run(lambda i: B.bl_gemm_tq2_0_int8(q, s, ws[i % cps], wl.N, y=y))
+        tops = 2.0 * Mq * wl.N * wl.K / (t * 1e-3) / 1e12
+        out["tq2_0_int8_5120x13824_M512"] = {"value": round(tops, 1), "unit": "TOPS (int8 ops)",
+                                             "frac_bf16_dense_peak": round(tops / bf16_peak, 4), "us_per_launch": t * 1e3}
+        del ws, p0, y
 
         # W1A8 LM head, M = 1, 4, 8
         wl = synth.WORKLOADS["w1a8_lmhead_248320"]
@@ -482,6 +491,13 @@ def bench_cublas(args, torch, stream, dist, run):
     t = run(lambda i: torch.matmul(xm, W[i % 8].t()))
     out["cublas_bf16_prefill_512"] = {"us_per_launch": t * 1e3, "unit": "us",
                                       "tflops": round(2.0 * 512 * 6912 * 2560 / (t * 1e-3) / 1e12, 1)}
+    del W, xm
+    # the TQ2_0 shape, M = 512
+    W = dense(13824, 5120, 4)
+    xm = torch.randn(512, 5120, device="cuda", dtype=torch.bfloat16, generator=gen)
+    t = run(lambda i: torch.matmul(xm, W[i % 4].t()))
+    out["cublas_bf16_5120x13824_M512"] = {"us_per_launch": t * 1e3, "unit": "us",
+                                          "tflops": round(2.0 * 512 * 13824 * 5120 / (t * 1e-3) / 1e12, 1)}
     del W, xm
     torch.cuda.empty_cache()
     return out

@@ -17,11 +17,13 @@ LIB_PATH = os.path.join(_HERE, "libbl.so")
 BL_OK, BL_ERR_NULL, BL_ERR_SHAPE, BL_ERR_ALIGN, BL_ERR_DTYPE, BL_ERR_UNSUPPORTED, BL_ERR_CUDA = range(7)
 BL_F32, BL_BF16 = 0, 1
 BL_DEVERR_WAIT_TIMEOUT = 0x1
+BL_DEVERR_RANGE = 0x2
 
 EXPORTS = [
     "bl_status_string", "bl_last_error", "bl_device_error", "bl_set_overlap", "bl_get_overlap",
     "bl_pack_i2s", "bl_pack_tq2_0", "bl_pack_w1", "bl_quantize_act_absmax_int8",
     "bl_gemv_i2s", "bl_gemv_i2s_residual", "bl_gemv_i2s_rmsnorm", "bl_gemv_i2s_gate_up", "bl_gemv_tq2_0", "bl_gemm_w1a8", "bl_gemm_w1a8_act", "bl_gemm_i2s_int8",
+    "bl_gemm_tq2_0_int8",
 ]
 
 
@@ -51,6 +53,7 @@ def _declare(L):
         "bl_gemm_w1a8": ([p, p, p, p, p, i64, i64, i64, i32, p, p, p], st),
         "bl_gemm_w1a8_act": ([p, i32, p, p, p, i64, i64, i64, i32, p, p], st),
         "bl_gemm_i2s_int8": ([p, p, p, i64, i64, i64, p, p, p], st),
+        "bl_gemm_tq2_0_int8": ([p, p, p, i64, i64, i64, p, p], st),
     }
     for name, (args, res) in sig.items():
         f = getattr(L, name)
@@ -282,3 +285,14 @@ def bl_gemm_i2s_int8(q, s, packed, N, y=None, acc=False, stream=None):
     _check(_lib.bl_gemm_i2s_int8(_ptr(q), _ptr(s), _ptr(packed), M, N, K, _ptr(_cuda(y, "y")), _ptr(a),
                                  _stream(stream)))
     return (y, a) if a is not None else y
+
+
+def bl_gemm_tq2_0_int8(q, s, packed, N, y=None, stream=None):
+    """y[m, n] = s[m] * sum_b d[n,b] * (block dot of w and q), fp32 [M, N]."""
+    for t, n in ((q, "q"), (s, "s"), (packed, "packed")):
+        _cuda(t, n)
+    M, K = q.shape
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float32, device=q.device)
+    _check(_lib.bl_gemm_tq2_0_int8(_ptr(q), _ptr(s), _ptr(packed), M, N, K, _ptr(_cuda(y, "y")), _stream(stream)))
+    return y

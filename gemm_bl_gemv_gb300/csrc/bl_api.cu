@@ -40,6 +40,31 @@ cudaStream_t S(bl_stream_t s) { return reinterpret_cast<cudaStream_t>(s); }
 
 bool overlap_enabled() { return g_overlap.load(std::memory_order_relaxed) != 0; }
 
+bool encode_tmap_2d_u8(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint64_t row_bytes,
+                       uint32_t box_inner, uint32_t box_outer, bool swizzle128) {
+  using Encode = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                              const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                              CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+  static Encode encode = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      encode = reinterpret_cast<Encode>(fn);
+  });
+  if (!encode || box_inner % 16 || box_inner == 0 || box_inner > 256 || box_outer == 0 || box_outer > 256 ||
+      row_bytes % 16 || inner == 0 || outer == 0 || inner >= (uint64_t(1) << 32) || outer >= (uint64_t(1) << 32))
+    return false;
+  const cuuint64_t dim[2] = {inner, outer}, stride[1] = {row_bytes};
+  const cuuint32_t boxd[2] = {box_inner, box_outer}, estr[2] = {1, 1};
+  return encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dim, stride, boxd, estr,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 unsigned int* dev_error_ptr() {
   static unsigned int* cache[64] = {nullptr};
   static std::mutex mu;
@@ -276,6 +301,19 @@ bl_status bl_gemm_w1a8_act(const void* x, bl_dtype xt, const int32_t* wq, const 
     return fail(BL_ERR_ALIGN, "bl_gemm_w1a8_act: x, wq, ws must be 16-byte aligned; y, bias 2-byte aligned");
   return cuda_status(launch_gemm_w1a8_act(x, xt, wq, ws_fp16, bias_bf16, M, N, K, group, y_bf16, S(stream)),
                      "bl_gemm_w1a8_act");
+}
+
+bl_status bl_gemm_tq2_0_int8(const int8_t* q, const float* s, const uint8_t* packed, int64_t M, int64_t N,
+                             int64_t K, float* y, bl_stream_t stream) {
+  if (!q || !s || !packed || !y) return fail(BL_ERR_NULL, "bl_gemm_tq2_0_int8: NULL pointer");
+  if (M < 1 || N < 1 || K < 256 || K % 256 || N > 0x7fffffff || M > 0x7fffffff)
+    return fail(BL_ERR_SHAPE, "bl_gemm_tq2_0_int8: need M, N >= 1, K %% 256 == 0 (M=%lld N=%lld K=%lld)",
+                (long long)M, (long long)N, (long long)K);
+  if (K > (int64_t(1) << 24) || N * (K / 256) * 66 >= (int64_t(1) << 31))
+    return fail(BL_ERR_UNSUPPORTED, "bl_gemm_tq2_0_int8: K <= 2^24 and a packed tensor under 2 GiB supported");
+  if (!aligned(q, 16) || !aligned(s, 4) || !aligned(packed, 16) || !aligned(y, 16))
+    return fail(BL_ERR_ALIGN, "bl_gemm_tq2_0_int8: q, packed and y must be 16-byte aligned, s 4-byte");
+  return cuda_status(launch_gemm_tq2_0_int8(q, s, packed, M, N, K, y, S(stream)), "bl_gemm_tq2_0_int8");
 }
 
 bl_status bl_gemm_i2s_int8(const int8_t* q, const float* s, const uint8_t* packed, int64_t M, int64_t N, int64_t K,

@@ -3,6 +3,7 @@
 #include <cstdint>
 #include <mutex>
 #include <utility>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "bl.h"
@@ -19,6 +20,14 @@ int sm_count();
 // BL_DEVERR_* bits read by bl_device_error()); kernels receive it as an
 // argument.  nullptr if it cannot be resolved.
 unsigned int* dev_error_ptr();
+
+// A 2-D tiled TMA descriptor over uint8 [outer][inner] at `base` (16-byte
+// aligned) with rows `row_bytes` apart (a multiple of 16), loading boxes of
+// box_outer rows x box_inner bytes (box_inner a multiple of 16, both at most
+// 256), optionally with the 128-byte swizzle; elements outside the tensor
+// read as zero.  Returns false if the driver rejects it.
+bool encode_tmap_2d_u8(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint64_t row_bytes,
+                       uint32_t box_inner, uint32_t box_outer, bool swizzle128);
 
 // Launch plans (geometry, grid, kernel attributes already set) remembered per
 // (device, N, K) so that repeated calls skip the occupancy queries.
@@ -110,6 +119,8 @@ cudaError_t launch_gemm_w1a8_act(const void* x, bl_dtype xt, const int32_t* wq, 
 cudaError_t launch_gemm_w1a8_act_tiled(const void* x, bl_dtype xt, const int32_t* wq, const uint16_t* ws,
                                        const uint16_t* bias, int64_t M, int64_t N, int64_t K, int group, uint16_t* y,
                                        cudaStream_t st);
+cudaError_t launch_gemm_tq2_0_int8(const int8_t* q, const float* s, const uint8_t* packed, int64_t M, int64_t N,
+                                   int64_t K, float* y, cudaStream_t st);
 cudaError_t launch_gemm_i2s_int8_simt(const int8_t* q, const float* sc, const uint8_t* packed, int64_t M, int64_t N,
                                       int64_t K, float* y, int32_t* acc, cudaStream_t s);
 cudaError_t launch_gemm_i2s_int8(const int8_t* q, const float* sc, const uint8_t* packed, int64_t M, int64_t N,

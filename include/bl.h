@@ -70,6 +70,7 @@ const char* bl_last_error(void);
  * clear != 0 resets it to zero.  Returns BL_ERR_CUDA if the read fails.
  */
 #define BL_DEVERR_WAIT_TIMEOUT 0x1u   /* a pipeline wait exceeded its limit */
+#define BL_DEVERR_RANGE 0x2u          /* an input value outside a kernel's stated range (see the entry point) */
 bl_status bl_device_error(uint32_t* flags, int clear);
 
 /*
@@ -265,6 +266,25 @@ bl_status bl_gemm_w1a8(const int8_t* q, const float* s, const int32_t* wq, const
 bl_status bl_gemm_w1a8_act(const void* x, bl_dtype xt, const int32_t* wq, const uint16_t* ws_fp16,
                            const uint16_t* bias_bf16, int64_t M, int64_t N, int64_t K, int group, uint16_t* y_bf16,
                            bl_stream_t stream);
+
+/*
+ * TQ2_0 product with int8 activations (large M) [TQ "TQ2_0 Format";
+ * activations as BG "quantize_activation"]:
+ *   y[m,n] = s[m] * sum_b f32(d[n,b]) * sum_{j<256} w[n,256b+j] q[m,256b+j]
+ *   q : int8 [M, K];  s : fp32 [M];  packed : TQ2_0 tensor (bl_pack_tq2_0).
+ *   y : fp32 [M, N].
+ * Runs on the tensor cores with exact fp16 operands (q scaled by 4^-(k%4),
+ * w*d by 4^(k%4)): every product is exactly q*w*d and the sum over K is
+ * fp32 in an order of the library's choosing.  Block scales must satisfy
+ * |d| < 1024 (fp16 subnormals included); a larger one sets BL_DEVERR_RANGE
+ * in the device error word and its rows of y are undefined.  Tiles are 128
+ * tokens: meant for M in the tens and above (one token is bl_gemv_tq2_0's
+ * job).
+ * Requires M, N >= 1, K % 256 == 0, K <= 2^24, a packed tensor under 2 GiB;
+ * q, packed and y 16-byte aligned, s 4-byte aligned.
+ */
+bl_status bl_gemm_tq2_0_int8(const int8_t* q, const float* s, const uint8_t* packed, int64_t M, int64_t N, int64_t K,
+                             float* y, bl_stream_t stream);
 
 /*
  * i2_s product with int8 activations (prefill, large M)

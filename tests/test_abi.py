@@ -56,6 +56,10 @@ def test_host_checks_without_gpu():
     assert L.bl_gemm_w1a8(fake, fake, fake, fake, None, 1, 4, 128, 48, fake, None, None) == B.BL_ERR_SHAPE
     assert L.bl_gemm_i2s_int8(fake, fake, fake, 4, 4, 132224, fake, None, None) == B.BL_ERR_UNSUPPORTED
     assert L.bl_gemm_w1a8_act(fake, 1, fake, fake, None, 9, 4, 1024, 128, fake, None) == B.BL_ERR_UNSUPPORTED
+    assert L.bl_gemm_tq2_0_int8(fake, fake, fake, 4, 4, 384, fake, None) == B.BL_ERR_SHAPE
+    assert L.bl_gemm_tq2_0_int8(fake, fake, fake, 0, 4, 256, fake, None) == B.BL_ERR_SHAPE
+    assert L.bl_gemm_tq2_0_int8(None, fake, fake, 4, 4, 256, fake, None) == B.BL_ERR_NULL
+    assert L.bl_gemm_tq2_0_int8(fake, fake, ctypes.c_void_p(16 * 1024 + 2), 4, 4, 256, fake, None) == B.BL_ERR_ALIGN
     assert L.bl_gemm_w1a8_act(fake, 1, fake, fake, None, 1, 4, 65536, 32, fake, None) == B.BL_ERR_UNSUPPORTED
     assert L.bl_gemm_w1a8_act(fake, 1, fake, fake, None, 1, 4, 1024, 48, fake, None) == B.BL_ERR_SHAPE
     assert L.bl_gemm_w1a8_act(fake, 5, fake, fake, None, 1, 4, 1024, 128, fake, None) == B.BL_ERR_DTYPE

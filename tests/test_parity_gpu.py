@@ -322,6 +322,59 @@ def test_gemv_tq2_0_workload(B):
     assert_close(y, ref, cond, TOL_F32, "tq2_0 workload")
 
 
+@pytest.mark.parametrize("M,N,K", [(1, 1, 256), (9, 70, 512), (128, 192, 1024), (130, 200, 2560),
+                                   (512, 96, 768), (257, 389, 5120)])
+def test_gemm_tq2_0_int8(B, M, N, K):
+    """TQ2_0 x int8 on the tensor cores: ragged M and N tails, N % 4 != 0
+    (per-element stores), a negative, a zero and a subnormal block scale."""
+    g = rng(5 * M + N + K)
+    w = ternary(g, N, K)
+    d = synth.abs_normal_fp16_bits(g, (N, K // 256), 0.02)
+    d[0, 0] = 0x0001  # fp16 subnormal
+    if N > 2:
+        d[1, :] = 0x8000 | d[1, :]  # negative scales
+        d[2, 0] = 0
+    xb = synth.f32_to_bf16_bits(synth.normal_f32(g, (M, K)))
+    q, s = O.quantize_act_absmax_int8(xb, "bf16")
+    packed = B.bl_pack_tq2_0(to_gpu(w), fp16_gpu(d))
+    y = B.bl_gemm_tq2_0_int8(to_gpu(q), to_gpu(s), packed, N).cpu().numpy().astype(np.float64)
+    ref, cond = O.gemm_tq2_0_int8(q, s, O.pack_tq2_0(w, d), N, K)
+    assert_close(y, ref, cond, TOL_F32, "tq2_0 int8 M=%d %dx%d" % (M, N, K))
+
+
+def test_gemm_tq2_0_int8_scale_range_flag(B):
+    """A block scale of 1024 or more is outside the kernel's exact range: the
+    launch completes, flags BL_DEVERR_RANGE, and the other rows stay exact."""
+    g = rng(4242)
+    M, N, K = 130, 40, 512
+    w = ternary(g, N, K)
+    d = synth.abs_normal_fp16_bits(g, (N, K // 256), 0.02)
+    d[7, 1] = 0x6800  # 2048
+    q, s = O.quantize_act_absmax_int8(synth.f32_to_bf16_bits(synth.normal_f32(g, (M, K))), "bf16")
+    B.device_error(clear=True)
+    y = B.bl_gemm_tq2_0_int8(to_gpu(q), to_gpu(s), B.bl_pack_tq2_0(to_gpu(w), fp16_gpu(d)), N)
+    torch.cuda.synchronize()
+    assert B.device_error(clear=True) & B.BL_DEVERR_RANGE
+    rows = np.array([r for r in range(N) if r != 7])
+    ref, cond = O.gemm_tq2_0_int8(q, s, O.pack_tq2_0(w, d), N, K, rows=rows)
+    assert_close(y.cpu().numpy().astype(np.float64)[:, rows], ref, cond, TOL_F32, "tq2_0 int8 other rows")
+
+
+def test_gemm_tq2_0_int8_workload(B):
+    """The 5120 -> 13824 TQ2_0 weights against 512 quantized tokens, sampled rows."""
+    wl = synth.WORKLOADS["tq2_0_gemv_5120x13824"]
+    M = 512
+    w = synth.weight_matrix(wl.index, "w", wl.N, wl.K, "ternary", wl.p_zero)
+    d = synth.block_scale_matrix(wl.index, wl.N, wl.K // 256)
+    xb = synth.activations(wl.index, M, wl.K, "bf16")
+    q, s = O.quantize_act_absmax_int8(xb, "bf16")
+    packed = B.bl_pack_tq2_0(to_gpu(w), fp16_gpu(d))
+    y = B.bl_gemm_tq2_0_int8(to_gpu(q), to_gpu(s), packed, wl.N).cpu().numpy().astype(np.float64)
+    rows = np.unique(np.concatenate([[0, 1, wl.N - 1, wl.N - 2], rng(11).integers(0, wl.N, 40)]))
+    ref, cond = O.gemm_tq2_0_int8(q, s, O.pack_tq2_0(w, d), wl.N, wl.K, rows=rows)
+    assert_close(y[:, rows], ref, cond, TOL_F32, "tq2_0 int8 workload")
+
+
 # ---------------------------------------------------------------------------
 # W1A8
 # ---------------------------------------------------------------------------
