@@ -271,7 +271,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (issuer) {
         bulk_s2g(y + int64_t(m0 + threadIdx.x) * N + n0, smem + threadIdx.x * kOutStride, uint32_t(ncols) * 2);
         bulk_commit();
-        bulk_wait();
+        bulk_wait_read();  // the global writes complete with the grid
       }
     } else if (m < M && ok) {
       for (int j = 0; j < 48; ++j) {
