@@ -206,7 +206,7 @@ def time_graph(torch, dist, body, steps, warmup, graph_steps, stream):
 def kernel_source_hash():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "gemm_bl_gemv_gb300", "csrc")
-    for f in ("gemv_i2s.cu", "bl_device.cuh", "bl_internal.h"):
+    for f in ("gemv_i2s.cu", "bl_device.cuh"):  # the kernel's device code
         h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:16]
 
@@ -447,7 +447,8 @@ def bench_secondary(args, B, torch, stream, dist, hbm, bf16_peak):
         out[wl.name] = {"value": round(tops, 2), "unit": "TOPS (int8 ops)", "frac_bf16_dense_peak": round(tops / bf16_peak, 4),
                         "us_per_launch": t * 1e3}
         del ws
-        out.update(bench_cublas(args, torch, stream, dist, run))
+        if not args.no_cublas:
+            out.update(bench_cublas(args, torch, stream, dist, run))
     torch.cuda.synchronize()
     return out
 
@@ -593,6 +594,7 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=20000)
     ap.add_argument("--secondary-steps", type=int, default=2000)
     ap.add_argument("--no-extra", action="store_true")
+    ap.add_argument("--no-cublas", action="store_true", help="skip the cuBLAS comparison column (5 GB of dense weights)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--ref-seconds", type=float, default=60.0)
     args = ap.parse_args()

@@ -3,7 +3,9 @@
 //
 // Work decomposition.  A warp owns a tile of 8 consecutive rows; four lanes
 // work on each row and take every fourth 256-element block; their sums are
-// added with two shuffles.  A tile is contiguous in memory (8 * 66 bytes per
+// added with two shuffles.  The grid has one CTA per SM and CTA b takes the
+// contiguous tile range [b T / G, (b + 1) T / G), so every SM decodes the
+// same number of tiles (to one), its warps taking them in turn.  A tile is contiguous in memory (8 * 66 bytes per
 // block, always a multiple of 16), so one thread bulk-copies it
 // (cp.async.bulk) into a ring buffer of the warp.  Blocks of odd index start
 // 2 bytes past a 4-byte boundary; their code words are assembled from two
@@ -109,7 +111,7 @@ __device__ __forceinline__ void prepare_x(const uint8_t* xraw, int nb, uint32_t*
 }
 
 template <int D, bool XB>
-__global__ void __launch_bounds__(256) gemv_tq2_0_kernel(const uint8_t* __restrict__ packed,
+__global__ void __launch_bounds__(512) gemv_tq2_0_kernel(const uint8_t* __restrict__ packed,
                                                          const void* __restrict__ x, float* __restrict__ y, Geom g,
                                                          int early_weights) {
   extern __shared__ __align__(128) uint8_t smem[];
@@ -125,9 +127,11 @@ __global__ void __launch_bounds__(256) gemv_tq2_0_kernel(const uint8_t* __restri
   uint8_t* xraw = smem + g.off_xraw;
   __shared__ int abort_flag;
 
-  const int tile_stride = int(gridDim.x) * nwarps;
-  const int first = int(blockIdx.x) * nwarps + warp;
-  const int my_tiles = first < g.ntiles ? (g.ntiles - 1 - first) / tile_stride + 1 : 0;
+  const int t0 = int(int64_t(blockIdx.x) * g.ntiles / gridDim.x);
+  const int t1 = int(int64_t(blockIdx.x + 1) * g.ntiles / gridDim.x);
+  const int tile_stride = nwarps;
+  const int first = t0 + warp;
+  const int my_tiles = first < t1 ? (t1 - 1 - first) / tile_stride + 1 : 0;
 
   auto issue = [&](int i) {  // lane 0 only
     const int t = first + i * tile_stride;
@@ -258,14 +262,14 @@ bool plan(Geom& g, int64_t N, int64_t K, int esize, int max_smem, int nsm) {
   g.ntiles = int((N + kRows - 1) / kRows);
   // + 4 bytes so the funnel-shift read of the last word stays inside the buffer
   g.stage_bytes = uint32_t(up(uint64_t(kRows) * g.row_bytes + 4, 128));
-  // warps per CTA: up to 8, fewer when tiles are few
-  int wpb = 8;
-  while (wpb > 1 && int64_t(g.ntiles) < int64_t(wpb) * nsm / 2) wpb /= 2;
-  g.wpb = wpb;
-  const int64_t tiles_per_warp = (g.ntiles + int64_t(wpb) * nsm - 1) / (int64_t(wpb) * nsm);
-  // prefer two CTAs per SM: the deepest ring that fits half the shared memory, else the whole
-  for (int half = 1; half >= 0; --half) {
-    const uint64_t lim = half ? uint64_t(max_smem) / 2 - 1024 : uint64_t(max_smem);
+  // one CTA per SM with an even share of the tiles; as many warps as tiles
+  // (at most 16), then the deepest ring that fits
+  const int64_t grid = std::min<int64_t>(g.ntiles, nsm);
+  const int64_t per_cta = (g.ntiles + grid - 1) / grid;
+  for (int wpb = int(std::min<int64_t>(16, per_cta)); wpb >= 1; --wpb) {
+    g.wpb = wpb;
+    const uint64_t lim = uint64_t(max_smem);
+    const int64_t tiles_per_warp = (per_cta + wpb - 1) / wpb;
     for (int st = int(std::min<int64_t>(3, std::max<int64_t>(1, tiles_per_warp))); st >= 1; --st) {
       uint64_t off = 0;
       g.off_bar = uint32_t(off);
@@ -306,11 +310,7 @@ cudaError_t run(const uint8_t* packed, const void* x, float* y, int64_t N, int64
     cudaError_t e = raise_smem_cap(kern, dev, max_optin - 1024);
     if (e != cudaSuccess) return e;
     p.threads = 32 * p.g.wpb;
-    int bps = 0;
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bps, kern, p.threads, p.g.smem);
-    if (bps < 1) bps = 1;
-    p.grid = (p.g.ntiles + p.g.wpb - 1) / p.g.wpb;
-    if (p.grid > nsm * bps) p.grid = nsm * bps;
+    p.grid = int(std::min<int64_t>(p.g.ntiles, nsm));
     p.g.err = dev_error_ptr();
     cache.put(dev, N, K, p);
   }
