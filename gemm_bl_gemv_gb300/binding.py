@@ -109,6 +109,24 @@ def _cuda(t, name):
     return t
 
 
+_cudart = None
+
+
+def cudart():
+    """The CUDA runtime libbl.so is linked against (same process-wide library),
+    with cudaMemcpyAsync declared, for callers that drive the C ABI directly."""
+    global _cudart
+    if _cudart is None:
+        rt = ctypes.CDLL("libcudart.so.13")
+        rt.cudaMemcpyAsync.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_void_p]
+        rt.cudaMemcpyAsync.restype = ctypes.c_int
+        _cudart = rt
+    return _cudart
+
+
+CUDA_MEMCPY_H2D, CUDA_MEMCPY_D2H = 1, 2
+
+
 def set_overlap(enable: bool):
     _lib.bl_set_overlap(1 if enable else 0)
 
