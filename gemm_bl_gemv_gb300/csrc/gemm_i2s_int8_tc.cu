@@ -39,7 +39,8 @@ namespace bl {
 namespace {
 
 constexpr int BM = 128, BN = 192, BK = 128;
-constexpr int kAWarps = 4;                    // activation warps, one per TMEM lane quarter
+constexpr int kAWarps = 4;                    // activation warps: TMEM lane quarter w % 4, classes of w / 4
+static_assert(kAWarps == 4 || kAWarps == 8, "one or two activation warps per TMEM lane quarter");
 constexpr int kBWarps = 12;                   // weight decoding warps
 constexpr int kProducers = 32 * (kAWarps + kBWarps);
 constexpr int kBThreads = 32 * kBWarps;
@@ -147,17 +148,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   pdl_wait();
 
   if (warp < kAWarps) {
-    // ------- activation converters: TMEM lane / tile row ra, all 128 K
-    //         elements of a block (classes t = 0..3; TMEM columns 16t..16t+15
-    //         hold class t) -------
-    const int ra = warp * 32 + lane;
-    uint32_t sc[4], bias[4];
-#pragma unroll
-    for (int t = 0; t < 4; ++t) {
-      sc[t] = f16x2_pow2(2 * t - 6);
-      bias[t] = hfma2(0x64806480u, sc[t], 0x80008000u) ^ 0x80008000u;  // -(1152 * scale)
-    }
-    const uint32_t a_taddr = tmem + (uint32_t(warp * 32) << 16) + kAcol;
+    // ------- activation converters: TMEM lane / tile row ra = 32 (w % 4) +
+    //         lane, classes t of a block with t % (kAWarps / 4) = w / 4
+    //         (TMEM columns 16t..16t+15 hold class t) -------
+    constexpr int kTStep = kAWarps / 4;
+    const int quarter = warp & 3, t0 = warp >> 2;
+    const int ra = quarter * 32 + lane;
+    const uint32_t a_taddr = tmem + (uint32_t(quarter * 32) << 16) + kAcol;
     for (int kb = 0; kb < nkb; ++kb) {
       const int st = kb % kStages;
       if (kb >= kStages && !*abort_flag &&
@@ -168,19 +165,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       // row ra of the swizzled tile: chunk c at 16 * (c ^ (ra % 8))
       const uint8_t* arow = araw + st * kAStage + ra * 128;
 #pragma unroll
-      for (int t = 0; t < 4; ++t) {  // chunks 2t, 2t+1 = class t
+      for (int tt = 0; tt < 4; tt += kTStep) {  // chunks 2t, 2t+1 = class t
+        const int t = tt + t0;
+        const uint32_t sc = f16x2_pow2(2 * t - 6);
+        const uint32_t bias = hfma2(0x64806480u, sc, 0x80008000u) ^ 0x80008000u;  // -(1152 * scale)
         uint4 v[2];
 #pragma unroll
         for (int i = 0; i < 2; ++i) v[i] = *reinterpret_cast<const uint4*>(arow + (((2 * t + i) ^ (ra & 7)) << 4));
-        if (t == 3) mbar_arrive(&raw_empty[st]);
+        if (tt + kTStep == 4) mbar_arrive(&raw_empty[st]);
         uint32_t o[16];
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
           const uint4 c = v[i];
-          i8x4_to_f16_scaled(c.x, sc[t], bias[t], o[8 * i + 0], o[8 * i + 1]);
-          i8x4_to_f16_scaled(c.y, sc[t], bias[t], o[8 * i + 2], o[8 * i + 3]);
-          i8x4_to_f16_scaled(c.z, sc[t], bias[t], o[8 * i + 4], o[8 * i + 5]);
-          i8x4_to_f16_scaled(c.w, sc[t], bias[t], o[8 * i + 6], o[8 * i + 7]);
+          i8x4_to_f16_scaled(c.x, sc, bias, o[8 * i + 0], o[8 * i + 1]);
+          i8x4_to_f16_scaled(c.y, sc, bias, o[8 * i + 2], o[8 * i + 3]);
+          i8x4_to_f16_scaled(c.z, sc, bias, o[8 * i + 4], o[8 * i + 5]);
+          i8x4_to_f16_scaled(c.w, sc, bias, o[8 * i + 6], o[8 * i + 7]);
         }
         tmem_st16(a_taddr + 64 * st + 16 * t, o);
       }
@@ -337,19 +337,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (issuer) bulk_wait_read();  // the global writes complete with the grid
-    } else if (m < M && ok) {
+    } else {
 #pragma unroll
       for (int g = 0; g < 3; ++g) {
         uint32_t v[16];
-        tmem_ld16(trow + 16 * g, v);
+        tmem_ld16(trow + 16 * g, v);  // warp-collective: every lane loads, only rows below M store
         tmem_ld_wait();
-        for (int j = 0; j < 16; ++j) {
-          const int n = n0 + c0 + 16 * g + j;
-          if (n < N) {
-            y[int64_t(m) * N + n] = __fmul_rn(__fmul_rn(__uint_as_float(v[j]), sm), sw);
-            if (acc_out) acc_out[int64_t(m) * N + n] = __float2int_rn(__uint_as_float(v[j]));
+        if (m < M && ok)
+          for (int j = 0; j < 16; ++j) {
+            const int n = n0 + c0 + 16 * g + j;
+            if (n < N) {
+              y[int64_t(m) * N + n] = __fmul_rn(__fmul_rn(__uint_as_float(v[j]), sm), sw);
+              if (acc_out) acc_out[int64_t(m) * N + n] = __float2int_rn(__uint_as_float(v[j]));
+            }
           }
-        }
       }
     }
   }

@@ -323,7 +323,7 @@ def test_gemv_tq2_0_workload(B):
 
 
 @pytest.mark.parametrize("M,N,K", [(1, 1, 256), (9, 70, 512), (128, 192, 1024), (130, 200, 2560),
-                                   (512, 96, 768), (257, 389, 5120)])
+                                   (512, 96, 768), (257, 389, 5120), (20, 1, 256), (130, 40, 16384)])
 def test_gemm_tq2_0_int8(B, M, N, K):
     """TQ2_0 x int8 on the tensor cores: ragged M and N tails, N % 4 != 0
     (per-element stores), a negative, a zero and a subnormal block scale."""
@@ -423,10 +423,12 @@ def test_gemm_w1a8_no_dots_matches_dots_variant(B):
 
 @pytest.mark.parametrize("M", [9, 64, 130, 512])
 @pytest.mark.parametrize("G", [32, 128, 256])
-@pytest.mark.parametrize("N,K", [(200, 1024), (70, 2560)])
+@pytest.mark.parametrize("N,K", [(200, 1024), (70, 2560), (1, 256), (33, 128)])
 def test_gemm_w1a8_large_m_tensor_cores(B, M, G, N, K):
     """M > 8 runs on the tensor cores (B = +-group scale in fp16); with and
-    without bias, against the oracle's fp64 product."""
+    without bias, against the oracle's fp64 product (N = 1, one K block)."""
+    if K % G:
+        pytest.skip("K not a multiple of G")
     g = rng(M * 31 + G + N + K)
     w = synth.signs(g, (N, K))
     xb = synth.f32_to_bf16_bits(synth.normal_f32(g, (M, K)))
@@ -517,8 +519,11 @@ def test_gemm_w1a8_act_workload_lmhead(B, M):
 # i2_s x int8 (prefill)
 # ---------------------------------------------------------------------------
 
-@pytest.mark.parametrize("M,N,K", [(1, 1, 128), (5, 70, 256), (128, 128, 1024), (130, 200, 2560), (512, 96, 384)])
+@pytest.mark.parametrize("M,N,K", [(1, 1, 128), (5, 70, 256), (63, 40, 512), (64, 7, 128), (128, 128, 1024),
+                                   (130, 200, 2560), (512, 96, 384), (200, 1, 256), (129, 385, 12800)])
 def test_gemm_i2s_int8_small(B, M, N, K):
+    """M < 64 runs on the CUDA cores, M >= 64 on the tensor cores (one K block,
+    N = 1, N % 4 != 0 with per-element stores, a ragged M tail, a long K)."""
     g = rng(M + N + K)
     w = ternary(g, N, K)
     q, s = O.quantize_act_absmax_int8(rand_x(g, K, "bf16", M), "bf16")
