@@ -76,27 +76,36 @@ def gate_up_algorithmic_bytes():
 # ---------------------------------------------------------------------------
 
 class Dist:
+    """One process per GPU (replicas: no data-path collective).  NCCL carries
+    the barrier and the max over ranks on GPUs; gloo does on a CPU-only host."""
+
     def __init__(self, n_gpus):
         self.world = int(os.environ.get("WORLD_SIZE", "1"))
         self.rank = int(os.environ.get("RANK", "0"))
         self.local = int(os.environ.get("LOCAL_RANK", "0"))
         self.pg = None
+        self.cuda = False
         if self.world > 1:
+            import torch
             import torch.distributed as dist
-            dist.init_process_group("nccl")
+            self.cuda = torch.cuda.is_available()
+            if self.cuda:
+                torch.cuda.set_device(self.local)
+            dist.init_process_group("nccl" if self.cuda else "gloo")
             self.pg = dist
 
     def barrier(self):
         if self.pg:
             import torch
             self.pg.barrier()
-            torch.cuda.synchronize()
+            if self.cuda:
+                torch.cuda.synchronize()
 
     def max(self, v):
         if not self.pg:
             return v
         import torch
-        t = torch.tensor([v], dtype=torch.float64, device="cuda")
+        t = torch.tensor([v], dtype=torch.float64, device="cuda" if self.cuda else "cpu")
         self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
         return float(t.item())
 
