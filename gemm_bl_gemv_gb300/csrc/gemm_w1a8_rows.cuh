@@ -389,7 +389,7 @@ cudaError_t run(const int8_t* q, const float* s, const void* x, const int32_t* w
   static PlanCache<Plan> cache;
   int dev = 0;
   cudaGetDevice(&dev);
-  Plan p;
+  Plan p{};
   if (!cache.get(dev, N, K * 4096 + G, &p)) {
     int max_optin = 0;
     cudaDeviceGetAttribute(&max_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);

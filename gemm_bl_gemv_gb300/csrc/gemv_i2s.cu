@@ -710,7 +710,7 @@ cudaError_t run(const uint8_t* packed, const uint8_t* packed2, const void* x, vo
   static PlanCache<Plan> cache;
   int dev = 0;
   cudaGetDevice(&dev);
-  Plan p;
+  Plan p{};
   if (!cache.get(dev, N, K, &p)) {
     int max_optin = 0;
     cudaDeviceGetAttribute(&max_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);

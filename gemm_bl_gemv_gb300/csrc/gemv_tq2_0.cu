@@ -301,7 +301,7 @@ cudaError_t run(const uint8_t* packed, const void* x, float* y, int64_t N, int64
   static PlanCache<Plan> cache;
   int dev = 0;
   cudaGetDevice(&dev);
-  Plan p;
+  Plan p{};
   if (!cache.get(dev, N, K, &p)) {
     int max_optin = 0;
     cudaDeviceGetAttribute(&max_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
