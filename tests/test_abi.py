@@ -71,3 +71,20 @@ def test_host_checks_without_gpu():
     assert L.bl_quantize_act_absmax_int8(fake, 3, 1, 8, fake, fake, None) == B.BL_ERR_DTYPE
     assert b"K % 128" in L.bl_last_error() or b"bl_" in L.bl_last_error()
     assert L.bl_status_string(B.BL_ERR_ALIGN) == b"BL_ERR_ALIGN"
+
+
+def test_binding_fails_loudly_without_the_library(tmp_path):
+    """No silent fallback: with libbl.so absent, importing the binding raises."""
+    import shutil
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    pkg = tmp_path / "gemm_bl_gemv_gb300"
+    pkg.mkdir()
+    for f in ("__init__.py", "binding.py"):
+        src = os.path.join(root, "gemm_bl_gemv_gb300", f)
+        if os.path.exists(src):
+            shutil.copy(src, pkg / f)
+    r = subprocess.run([sys.executable, "-c", "import gemm_bl_gemv_gb300.binding"], cwd=str(tmp_path),
+                       capture_output=True, text=True, timeout=300)
+    assert r.returncode != 0 and "ImportError" in r.stderr and "libbl.so" in r.stderr
