@@ -29,11 +29,11 @@
 // TQ2_0 block.
 //
 // Structure: one CTA per 128 x 192 output tile, K in blocks of 128, a
-// 3-stage pipeline.  Warp 17 issues the activation TMA loads; warps 0-3
-// convert the activations and write them to tensor memory with tcgen05.st
-// (the MMA reads A from TMEM); warps 4-15 decode the weights into the K-major
-// 128-byte-swizzled B operand in shared memory; one lane of warp 16 issues
-// eight 128x192x16 MMAs per block; warps 0-15 run the epilogue (fp32 tile
+// 3-stage pipeline.  Warps 0-3 convert the activations and write them to
+// tensor memory with tcgen05.st (the MMA reads A from TMEM); warps 4-19
+// decode the weights into the K-major 128-byte-swizzled B operand in shared
+// memory; one lane of warp 20 issues eight 128x192x16 MMAs per block; warp 21
+// issues the activation TMA loads; warps 0-15 run the epilogue (fp32 tile
 // staged in shared memory, one bulk copy per row).  Every wait is bounded.
 #include "bl_device.cuh"
 #include "bl_internal.h"
@@ -42,12 +42,15 @@ namespace bl {
 namespace {
 
 constexpr int BM = 128, BN = 192, BK = 128;
-constexpr int kProducers = 512;  // warps 0..15
-constexpr int kAWarps = 4;       // activation warps, one per TMEM lane quarter
-constexpr int kBThreads = kProducers - 32 * kAWarps;
+constexpr int kAWarps = 4;                    // activation warps, one per TMEM lane quarter
+constexpr int kBWarps = 16;                   // weight decoding warps
+constexpr int kProducers = 32 * (kAWarps + kBWarps);
+constexpr int kBThreads = 32 * kBWarps;
 constexpr int kChunks = BN * (BK / 8) / kBThreads;  // 16-byte B chunks per decoding thread and block
 static_assert(kChunks * kBThreads == BN * (BK / 8), "chunks must divide evenly");
-constexpr int kThreads = 576;    // + warp 16 (TMEM, MMA issue) + warp 17 (activation TMA)
+constexpr int kMmaWarp = kAWarps + kBWarps;   // TMEM allocation, MMA issue
+constexpr int kThreads = 32 * (kMmaWarp + 2);  // + one warp of activation TMA loads
+constexpr int kEpilogue = 512;                // warps 0..15 run the epilogue
 constexpr int kStages = 3;
 constexpr uint32_t kBStage = BN * BK * 2;  // 48 KB: two 64-column sub-tiles
 constexpr uint32_t kAStage = BM * BK;      // 16 KB of int8 activations, 128-byte swizzled
@@ -139,7 +142,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     *abort_flag = 0;
     fence_barrier_init();
   }
-  if (warp == 16) {
+  if (warp == kMmaWarp) {
     tmem_alloc(tmem_slot, kTmemCols);
     tmem_relinquish();
   }
@@ -185,7 +188,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       mbar_arrive(&full[st]);
     }
-  } else if (warp < 16) {
+  } else if (warp < kMmaWarp) {
     // ------- weight decoders: chunk g = tb + kBThreads i of a block is
     //         row g / 16, elements 8 (g % 16) .. 8 (g % 16) + 7 -------
     const int tb = threadIdx.x - 32 * kAWarps;
@@ -243,7 +246,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (kb + 1 < nkb) produce(kb + 1, c1, d1);
     }
     if (dmax >= 0x6400u && err) atomicOr(err, BL_DEVERR_RANGE);  // |d| >= 1024: w d S may overflow fp16
-  } else if (warp == 16) {
+  } else if (warp == kMmaWarp) {
     if (lane == 0) {
       // ---------------- MMA issue (one thread) ----------------
       const uint32_t sbase = smem_addr(smem);
@@ -313,7 +316,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         *reinterpret_cast<float4*>(stage_row + j) = o;
       }
       fence_async_smem();
-      named_barrier_sync(1, kProducers);
+      named_barrier_sync(1, kEpilogue);
       const bool issuer = threadIdx.x < BM && m0 + int(threadIdx.x) < M && ok;
       if (issuer) {
         bulk_s2g(y + int64_t(m0 + threadIdx.x) * N + n0, smem + threadIdx.x * kOutStride, uint32_t(ncols) * 4);
@@ -330,7 +333,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 16) {
+  if (warp == kMmaWarp) {
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
