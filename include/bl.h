@@ -47,7 +47,7 @@ typedef enum {
                               not a multiple the format requires              */
   BL_ERR_ALIGN = 3,        /* a pointer is not aligned as documented          */
   BL_ERR_DTYPE = 4,        /* an unsupported bl_dtype value                   */
-  BL_ERR_UNSUPPORTED = 5,  /* valid request outside what this build supports  */
+  BL_ERR_UNSUPPORTED = 5,  /* valid request outside what the library supports */
   BL_ERR_CUDA = 6          /* the CUDA runtime reported an error              */
 } bl_status;
 
