@@ -183,20 +183,6 @@ bl_status bl_quantize_act_absmax_int8(const void* x, bl_dtype xt, int64_t M, int
   return cuda_status(launch_act_quant(x, xt, M, K, q, s, S(stream)), "bl_quantize_act_absmax_int8");
 }
 
-bl_status bl_gemv_i2s(const uint8_t* packed, const void* x, bl_dtype xt, void* y, bl_dtype yt, int64_t N, int64_t K,
-                      bl_stream_t stream) {
-  if (!packed || !x || !y) return fail(BL_ERR_NULL, "bl_gemv_i2s: NULL pointer");
-  if ((xt != BL_F32 && xt != BL_BF16) || (yt != BL_F32 && yt != BL_BF16))
-    return fail(BL_ERR_DTYPE, "bl_gemv_i2s: bad dtype (x %d, y %d)", int(xt), int(yt));
-  if (N < 1 || K < 128 || K % 128 || N > 0x7fffffff)
-    return fail(BL_ERR_SHAPE, "bl_gemv_i2s: need N >= 1, K %% 128 == 0 (N=%lld K=%lld)", (long long)N, (long long)K);
-  if (K > 32768) return fail(BL_ERR_UNSUPPORTED, "bl_gemv_i2s: K up to 32768 supported (K=%lld)", (long long)K);
-  if (!aligned(packed, 16)) return fail(BL_ERR_ALIGN, "bl_gemv_i2s: packed must be 16-byte aligned");
-  if (!aligned(x, xt == BL_F32 ? 4 : 2) || !aligned(y, yt == BL_F32 ? 4 : 2))
-    return fail(BL_ERR_ALIGN, "bl_gemv_i2s: x and y must be aligned to their element size");
-  return cuda_status(launch_gemv_i2s(packed, x, xt, y, yt, N, K, S(stream)), "bl_gemv_i2s");
-}
-
 static bl_status check_gemv_i2s(const char* fn, const uint8_t* packed, const void* x, bl_dtype xt, const void* y,
                                 bl_dtype yt, int64_t N, int64_t K) {
   if (!packed || !x || !y) return fail(BL_ERR_NULL, "%s: NULL pointer", fn);
@@ -209,6 +195,13 @@ static bl_status check_gemv_i2s(const char* fn, const uint8_t* packed, const voi
   if (!aligned(x, xt == BL_F32 ? 4 : 2) || !aligned(y, yt == BL_F32 ? 4 : 2))
     return fail(BL_ERR_ALIGN, "%s: x and y must be aligned to their element size", fn);
   return BL_OK;
+}
+
+bl_status bl_gemv_i2s(const uint8_t* packed, const void* x, bl_dtype xt, void* y, bl_dtype yt, int64_t N, int64_t K,
+                      bl_stream_t stream) {
+  const bl_status st = check_gemv_i2s("bl_gemv_i2s", packed, x, xt, y, yt, N, K);
+  if (st != BL_OK) return st;
+  return cuda_status(launch_gemv_i2s(packed, x, xt, y, yt, N, K, S(stream)), "bl_gemv_i2s");
 }
 
 bl_status bl_gemv_i2s_residual(const uint8_t* packed, const void* x, bl_dtype xt, const void* residual, void* y,
