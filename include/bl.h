@@ -67,7 +67,8 @@ const char* bl_last_error(void);
 /*
  * Read the library's device error word (synchronizes the device).
  * *flags receives the OR of BL_DEVERR_* bits recorded since the last clear;
- * clear != 0 resets it to zero.  Returns BL_ERR_CUDA if the read fails.
+ * clear != 0 resets it to zero.  Returns BL_ERR_NULL if flags is NULL and
+ * BL_ERR_CUDA if the read fails.
  */
 #define BL_DEVERR_WAIT_TIMEOUT 0x1u   /* a pipeline wait exceeded its limit */
 #define BL_DEVERR_RANGE 0x2u          /* an input value outside a kernel's stated range (see the entry point) */
@@ -116,7 +117,7 @@ bl_status bl_pack_i2s(const int8_t* w, float scale, int64_t N, int64_t K, uint8_
  *            order is this library's reading of the page, which prints the
  *            code table and the 2*idx shift of its unpack helper but not the
  *            element order.
- * Requires K % 256 == 0, N >= 1; `out` 2-byte aligned.
+ * Requires K % 256 == 0, N >= 1; `out` and `d_fp16` 2-byte aligned.
  */
 bl_status bl_pack_tq2_0(const int8_t* w, const uint16_t* d_fp16, int64_t N, int64_t K, uint8_t* out,
                         bl_stream_t stream);
@@ -145,7 +146,8 @@ bl_status bl_pack_w1(const int8_t* w, int64_t N, int64_t K, int32_t* out, bl_str
  * (The card states only "per-token absmax" with under 1% reconstruction
  * error; this formula is the library's reading and meets that bound.)
  *   q : int8 [M, K];  s : fp32 [M].
- * Requires M >= 1, K >= 1.  x must be aligned to its element size.
+ * Requires M >= 1, K >= 1.  x must be aligned to its element size, s to 4
+ * bytes.
  * Non-finite inputs give unspecified q and s.
  */
 bl_status bl_quantize_act_absmax_int8(const void* x, bl_dtype xt, int64_t M, int64_t K, int8_t* q, float* s,
@@ -223,7 +225,8 @@ bl_status bl_gemv_i2s_gate_up(const uint8_t* packed_gate, const uint8_t* packed_
  *   packed : as written by bl_pack_tq2_0.  x : [K] fp32 or bf16.  y : fp32 [N].
  * Accuracy as for bl_gemv_i2s (fp32 output), with one fixed-point exponent
  * per 256-element block.
- * Requires K % 256 == 0, N >= 1; `packed` 16-byte aligned.
+ * Requires K % 256 == 0, N >= 1; K <= 262144 (BL_ERR_UNSUPPORTED above);
+ * `packed` 16-byte aligned, x and y aligned to their element size.
  */
 bl_status bl_gemv_tq2_0(const uint8_t* packed, const void* x, bl_dtype xt, float* y, int64_t N, int64_t K,
                         bl_stream_t stream);
@@ -245,7 +248,9 @@ bl_status bl_gemv_tq2_0(const uint8_t* packed, const void* x, bl_dtype xt, float
  * on the tensor cores with B = +-ws (exact fp16), every product exact and
  * the sum over K in fp32 (group_dots must then be NULL, and K % 128 == 0).
  * Requires M >= 1, K % 32 == 0, group % 32 == 0, K % group == 0, N >= 1;
- * q, wq, ws 16-byte aligned.
+ * at most 1024 groups per row, and for M > 8 K <= 132096 (BL_ERR_UNSUPPORTED
+ * otherwise); q, wq, ws 16-byte aligned, the other pointers aligned to
+ * their element size.
  */
 bl_status bl_gemm_w1a8(const int8_t* q, const float* s, const int32_t* wq, const uint16_t* ws_fp16,
                        const uint16_t* bias_bf16, int64_t M, int64_t N, int64_t K, int group, uint16_t* y_bf16,

@@ -88,3 +88,87 @@ def test_binding_fails_loudly_without_the_library(tmp_path):
     r = subprocess.run([sys.executable, "-c", "import gemm_bl_gemv_gb300.binding"], cwd=str(tmp_path),
                        capture_output=True, text=True, timeout=300)
     assert r.returncode != 0 and "ImportError" in r.stderr and "libbl.so" in r.stderr
+
+
+def test_every_documented_rejection_without_gpu():
+    """Each entry point's documented failure classes (include/bl.h), checked
+    one by one on the host: a failing check returns its status before any CUDA
+    call, so none of these touches a device."""
+    from gemm_bl_gemv_gb300 import build
+    build.build()
+    from gemm_bl_gemv_gb300 import binding as B
+    L = B.lib()
+    A = 16 * 1024                # 16-byte aligned, never dereferenced
+    P = ctypes.c_void_p
+    a, o2, o4, o8 = P(A), P(A + 2), P(A + 4), P(A + 8)
+    NULL, ERR, F32, BF16 = B.BL_ERR_NULL, B.BL_ERR_SHAPE, B.BL_F32, B.BL_BF16
+    AL, DT, UN = B.BL_ERR_ALIGN, B.BL_ERR_DTYPE, B.BL_ERR_UNSUPPORTED
+    cases = [
+        # bl_device_error
+        (L.bl_device_error, (None, 0), NULL),
+        # packing
+        (L.bl_pack_i2s, (None, 1.0, 4, 128, a, None), NULL),
+        (L.bl_pack_i2s, (a, 1.0, 0, 128, a, None), ERR),
+        (L.bl_pack_i2s, (a, 1.0, 4, 192, a, None), ERR),
+        (L.bl_pack_i2s, (a, 1.0, 4, 128, o8, None), AL),
+        (L.bl_pack_tq2_0, (a, None, 4, 256, a, None), NULL),
+        (L.bl_pack_tq2_0, (a, a, 4, 384, a, None), ERR),
+        (L.bl_pack_tq2_0, (a, P(A + 1), 4, 256, a, None), AL),
+        (L.bl_pack_tq2_0, (a, a, 4, 256, P(A + 1), None), AL),
+        (L.bl_pack_w1, (a, 4, 32, None, None), NULL),
+        (L.bl_pack_w1, (a, 0, 32, a, None), ERR),
+        (L.bl_pack_w1, (a, 4, 32, o2, None), AL),
+        # act-quant
+        (L.bl_quantize_act_absmax_int8, (a, F32, 1, 8, a, None, None), NULL),
+        (L.bl_quantize_act_absmax_int8, (a, F32, 0, 8, a, a, None), ERR),
+        (L.bl_quantize_act_absmax_int8, (a, F32, 1, 0, a, a, None), ERR),
+        (L.bl_quantize_act_absmax_int8, (o2, F32, 1, 8, a, a, None), AL),
+        (L.bl_quantize_act_absmax_int8, (a, BF16, 1, 8, a, o2, None), AL),
+        # i2_s GEMV family
+        (L.bl_gemv_i2s, (a, a, F32, a, 9, 4, 128, None), DT),
+        (L.bl_gemv_i2s, (a, a, F32, a, F32, 0, 128, None), ERR),
+        (L.bl_gemv_i2s, (a, a, F32, a, F32, 4, 32896, None), UN),
+        (L.bl_gemv_i2s, (a, o2, F32, a, F32, 4, 128, None), AL),
+        (L.bl_gemv_i2s_residual, (a, a, F32, None, a, F32, 4, 128, None), NULL),
+        (L.bl_gemv_i2s_residual, (a, a, F32, o2, a, F32, 4, 128, None), AL),
+        (L.bl_gemv_i2s_residual, (a, a, F32, a, a, F32, 4, 100, None), ERR),
+        (L.bl_gemv_i2s_rmsnorm, (a, a, F32, None, 1e-6, None, a, F32, 4, 128, None), NULL),
+        (L.bl_gemv_i2s_rmsnorm, (a, a, F32, a, -1.0, None, a, F32, 4, 128, None), ERR),
+        (L.bl_gemv_i2s_rmsnorm, (a, a, F32, a, float("nan"), None, a, F32, 4, 128, None), ERR),
+        (L.bl_gemv_i2s_rmsnorm, (a, a, BF16, P(A + 1), 1e-6, None, a, F32, 4, 128, None), AL),
+        (L.bl_gemv_i2s_rmsnorm, (a, a, F32, a, 1e-6, o2, a, F32, 4, 128, None), AL),
+        (L.bl_gemv_i2s_gate_up, (a, None, a, F32, a, F32, 4, 128, None), NULL),
+        (L.bl_gemv_i2s_gate_up, (a, a, a, 2, a, F32, 4, 128, None), DT),
+        (L.bl_gemv_i2s_gate_up, (a, a, a, F32, a, F32, 4, 65536, None), UN),
+        (L.bl_gemv_i2s_gate_up, (a, o8, a, F32, a, F32, 4, 128, None), AL),
+        # TQ2_0 GEMV
+        (L.bl_gemv_tq2_0, (None, a, F32, a, 4, 256, None), NULL),
+        (L.bl_gemv_tq2_0, (a, a, 3, a, 4, 256, None), DT),
+        (L.bl_gemv_tq2_0, (a, a, F32, a, 4, 256 * 1025, None), UN),
+        (L.bl_gemv_tq2_0, (a, a, F32, o2, 4, 256, None), AL),
+        # W1A8
+        (L.bl_gemm_w1a8, (a, a, a, a, None, 1, 4, 32 * 1025, 32, a, None, None), UN),
+        (L.bl_gemm_w1a8, (a, a, a, a, None, 9, 4, 132224, 128, a, None, None), UN),
+        (L.bl_gemm_w1a8, (a, a, a, a, None, 1, 0, 128, 128, a, None, None), ERR),
+        (L.bl_gemm_w1a8, (a, a, a, a, None, 1, 4, 128, 96, a, None, None), ERR),
+        (L.bl_gemm_w1a8, (o8, a, a, a, None, 1, 4, 128, 128, a, None, None), AL),
+        (L.bl_gemm_w1a8, (a, a, a, o8, None, 1, 4, 128, 128, a, None, None), AL),
+        (L.bl_gemm_w1a8, (a, a, a, a, P(A + 1), 1, 4, 128, 128, a, None, None), AL),
+        (L.bl_gemm_w1a8, (a, None, a, a, None, 1, 4, 128, 128, a, None, None), NULL),
+        (L.bl_gemm_w1a8_act, (a, F32, a, a, None, 1, 4, 128, 128, None, None), NULL),
+        (L.bl_gemm_w1a8_act, (a, F32, a, a, None, 1, 4, 128, 128, P(A + 1), None), AL),
+        # large-M products
+        (L.bl_gemm_tq2_0_int8, (a, a, a, 4, 4, (1 << 24) + 256, a, None), UN),
+        (L.bl_gemm_tq2_0_int8, (a, a, a, 4, 1 << 20, 1 << 16, a, None), UN),  # packed tensor >= 2 GiB
+        (L.bl_gemm_tq2_0_int8, (a, o2, a, 4, 4, 256, a, None), AL),
+        (L.bl_gemm_tq2_0_int8, (a, a, a, 4, 4, 256, o4, None), AL),
+        (L.bl_gemm_i2s_int8, (a, a, None, 4, 4, 128, a, None, None), NULL),
+        (L.bl_gemm_i2s_int8, (a, a, a, 4, 0, 128, a, None, None), ERR),
+        (L.bl_gemm_i2s_int8, (a, a, a, 4, 4, 192, a, None, None), ERR),
+        (L.bl_gemm_i2s_int8, (a, o4, a, 4, 4, 128, a, None, None), AL),
+        (L.bl_gemm_i2s_int8, (a, a, a, 4, 4, 128, a, o4, None), AL),
+    ]
+    for fn, args, want in cases:
+        got = fn(*args)
+        assert got == want, (fn.__name__, args, B.status_name(got), B.status_name(want), L.bl_last_error())
+        assert L.bl_last_error()  # every rejection leaves a message
