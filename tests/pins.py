@@ -428,6 +428,30 @@ def pin_w1a8_unit_scales_exact():
     assert np.array_equal(yb[sel], acc[sel].astype(np.float64)), "w1a8 unit scales exact"
 
 
+def pin_w1a8_full_path_within_bf16_step():
+    """From unquantized activations: act-quant, the W1A8 product and the bf16
+    output together stay within 2^-8 normwise of a dequantize-and-fp32
+    reference (weights w*ws, activations q*s), the bf16 rounding step
+    ("binary-gemm", "Correctness"); checked at group sizes 32 to 256."""
+    g = np.random.Generator(np.random.PCG64(31))
+    for G in (32, 64, 128, 256):
+        M, N, K = 4, 96, 1024
+        x = g.standard_normal((M, K)).astype(np.float32)
+        q, s = O.quantize_act_absmax_int8(x, "f32")
+        w = (g.integers(0, 2, size=(N, K), dtype=np.int8) * 2 - 1).astype(np.int8)
+        ws = (np.abs(g.standard_normal((N, K // G))) * 0.02).astype(np.float16)
+        _, y, _ = O.gemm_w1a8(q, s, O.pack_w1(w), ws.view(np.uint16), None, K, G)
+        yb = O.bf16_to_f64(O.round_bf16(y))
+        w_deq = w.astype(np.float32) * np.repeat(ws.astype(np.float32), G, axis=1)
+        x_deq = q.astype(np.float32) * s[:, None]
+        ref = (x_deq @ w_deq.T).astype(np.float64)
+        err = np.linalg.norm(yb - ref) / np.linalg.norm(ref)
+        assert err < 2.0 ** -8, "w1a8 full path normwise %.3g, G=%d" % (err, G)
+        # and the bound is not vacuous: without the group scales it fails
+        _, y1, _ = O.gemm_w1a8(q, s, O.pack_w1(w), np.full((N, K // G), 0x3C00, np.uint16), None, K, G)
+        assert np.linalg.norm(y1 - ref) / np.linalg.norm(ref) > 1.0
+
+
 def pin_fp16_decode_all_patterns():
     h = np.arange(65536, dtype=np.uint32).astype(np.uint16)
     ref = fp16_np(h)
