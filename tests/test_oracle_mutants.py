@@ -68,6 +68,13 @@ MUTANTS = {
     "fp16_bias": [("v = ldexp((double)(1024 + m), e - 25);", "v = ldexp((double)(1024 + m), e - 24);")],
     "bf16_subnormal": [("v = ldexp((double)m, -133);", "v = ldexp((double)m, -134);")],
     "bf16_round_ties_away": [("double r = nearbyint(ldexp(f, 8));", "double r = round(ldexp(f, 8));")],
+    "i2s_code_not_centered": [("acc += (double)w * x[e];", "acc += (double)(w + 1) * x[e];")],
+    "i2s_int8_code_not_centered": [("acc += (int64_t)q[m * K + k] * w;", "acc += (int64_t)q[m * K + k] * (w + 1);")],
+    "gate_up_dropped_relu": [("const double a = g[r] > 0.0 ? g[r] : 0.0;", "const double a = g[r];")],
+    "w1a8_dropped_token_scale": [("y[m * nrows + r] = sm * acc + b;", "y[m * nrows + r] = acc + b;")],
+    "w1a8_next_group_scale": [("const double wsg = orc_fp16_to_double(ws[n * ng + g]);",
+                               "const double wsg = orc_fp16_to_double(ws[n * ng + (g + 1) % ng]);")],
+    "act_amax_signed": [("const float a = fabsf(v);", "const float a = v;")],
 }
 
 
