@@ -75,6 +75,7 @@ MUTANTS = {
     "w1a8_next_group_scale": [("const double wsg = orc_fp16_to_double(ws[n * ng + g]);",
                                "const double wsg = orc_fp16_to_double(ws[n * ng + (g + 1) % ng]);")],
     "act_amax_signed": [("const float a = fabsf(v);", "const float a = v;")],
+    "act_in_double": [("volatile float t = v * inv;", "volatile float t = (float)((double)v * (127.0 / (double)amax));")],
     "norm_not_inverted": [("inv = 1.0 / sqrt(ss / (double)K + eps);", "inv = sqrt(ss / (double)K + eps);")],
     "residual_scaled": [("y[r] += residual[rows ? rows[r] : r];", "y[r] = (y[r] + residual[rows ? rows[r] : r]) * 2.0;")],
     "w1a8_bias_scaled": [("y[m * nrows + r] = sm * acc + b;", "y[m * nrows + r] = sm * (acc + b);")],
