@@ -410,6 +410,12 @@ def pin_w1a8_identity_and_matmul():
             if b is not None:
                 ref = ref + bf16_torch(b)[None, :]
             assert np.allclose(y, ref, rtol=1e-13, atol=1e-15), "w1a8 y, G=%d" % G
+            # the tolerance's condition number: |s| sum_k |ws_g(k)| |w_k| |q_k| + |bias| (|w| = 1)
+            qabs = np.abs(q.astype(np.float64)).reshape(M, K // G, G).sum(-1)
+            refc = np.abs(s[:, None].astype(np.float64)) * (qabs @ np.abs(wsd).T)
+            if b is not None:
+                refc = refc + np.abs(bf16_torch(b))[None, :]
+            assert np.allclose(cond, refc, rtol=1e-13), "w1a8 cond, G=%d" % G
 
 
 def pin_w1a8_unit_scales_exact():

@@ -75,6 +75,10 @@ MUTANTS = {
     "w1a8_next_group_scale": [("const double wsg = orc_fp16_to_double(ws[n * ng + g]);",
                                "const double wsg = orc_fp16_to_double(ws[n * ng + (g + 1) % ng]);")],
     "act_amax_signed": [("const float a = fabsf(v);", "const float a = v;")],
+    "w1a8_cond_without_bias": [("if (cond) cond[m * nrows + r] = fabs(sm) * c + fabs(b);",
+                                "if (cond) cond[m * nrows + r] = fabs(sm) * c;")],
+    "gate_up_cond_first_term_dropped": [("if (cond) cond[r] = 2.0 * a * fabs(u[r]) * cg[r] + a * a * cu[r];",
+                                         "if (cond) cond[r] = a * a * cu[r];")],
     "act_in_double": [("volatile float t = v * inv;", "volatile float t = (float)((double)v * (127.0 / (double)amax));")],
     "norm_not_inverted": [("inv = 1.0 / sqrt(ss / (double)K + eps);", "inv = sqrt(ss / (double)K + eps);")],
     "residual_scaled": [("y[r] += residual[rows ? rows[r] : r];", "y[r] = (y[r] + residual[rows ? rows[r] : r]) * 2.0;")],
