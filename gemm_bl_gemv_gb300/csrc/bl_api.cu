@@ -33,6 +33,16 @@ bl_status cuda_status(cudaError_t e, const char* what) {
   return fail(BL_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
 }
 
+// Status of a product launcher.  The launchers return cudaErrorInvalidConfiguration
+// or cudaErrorNotSupported, before any CUDA call, when a shape passed the checks
+// here but no launch plan exists for it: a tile, the activation records or x do not
+// fit in a CTA's shared memory, or no tensor map describes the operands.
+bl_status launch_status(cudaError_t e, const char* what) {
+  if (e == cudaErrorInvalidConfiguration || e == cudaErrorNotSupported)
+    return fail(BL_ERR_UNSUPPORTED, "%s: no launch plan for this shape (shared memory or tensor map limits)", what);
+  return cuda_status(e, what);
+}
+
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 cudaStream_t S(bl_stream_t s) { return reinterpret_cast<cudaStream_t>(s); }
@@ -201,7 +211,7 @@ bl_status bl_gemv_i2s(const uint8_t* packed, const void* x, bl_dtype xt, void* y
                       bl_stream_t stream) {
   const bl_status st = check_gemv_i2s("bl_gemv_i2s", packed, x, xt, y, yt, N, K);
   if (st != BL_OK) return st;
-  return cuda_status(launch_gemv_i2s(packed, x, xt, y, yt, N, K, S(stream)), "bl_gemv_i2s");
+  return launch_status(launch_gemv_i2s(packed, x, xt, y, yt, N, K, S(stream)), "bl_gemv_i2s");
 }
 
 bl_status bl_gemv_i2s_residual(const uint8_t* packed, const void* x, bl_dtype xt, const void* residual, void* y,
@@ -211,8 +221,8 @@ bl_status bl_gemv_i2s_residual(const uint8_t* packed, const void* x, bl_dtype xt
   if (!residual) return fail(BL_ERR_NULL, "bl_gemv_i2s_residual: residual is NULL");
   if (!aligned(residual, yt == BL_F32 ? 4 : 2))
     return fail(BL_ERR_ALIGN, "bl_gemv_i2s_residual: residual must be aligned to its element size");
-  return cuda_status(launch_gemv_i2s(packed, x, xt, y, yt, N, K, S(stream), residual, nullptr, 0.f),
-                     "bl_gemv_i2s_residual");
+  return launch_status(launch_gemv_i2s(packed, x, xt, y, yt, N, K, S(stream), residual, nullptr, 0.f),
+                       "bl_gemv_i2s_residual");
 }
 
 bl_status bl_gemv_i2s_rmsnorm(const uint8_t* packed, const void* x, bl_dtype xt, const void* rms_weight, float eps,
@@ -223,8 +233,8 @@ bl_status bl_gemv_i2s_rmsnorm(const uint8_t* packed, const void* x, bl_dtype xt,
   if (!aligned(rms_weight, xt == BL_F32 ? 4 : 2) || (residual && !aligned(residual, yt == BL_F32 ? 4 : 2)))
     return fail(BL_ERR_ALIGN, "bl_gemv_i2s_rmsnorm: rms_weight / residual must be aligned to their element size");
   if (!(eps >= 0.f)) return fail(BL_ERR_SHAPE, "bl_gemv_i2s_rmsnorm: eps must be >= 0");
-  return cuda_status(launch_gemv_i2s(packed, x, xt, y, yt, N, K, S(stream), residual, rms_weight, eps),
-                     "bl_gemv_i2s_rmsnorm");
+  return launch_status(launch_gemv_i2s(packed, x, xt, y, yt, N, K, S(stream), residual, rms_weight, eps),
+                       "bl_gemv_i2s_rmsnorm");
 }
 
 bl_status bl_gemv_i2s_gate_up(const uint8_t* packed_gate, const uint8_t* packed_up, const void* x, bl_dtype xt,
@@ -240,8 +250,8 @@ bl_status bl_gemv_i2s_gate_up(const uint8_t* packed_gate, const uint8_t* packed_
     return fail(BL_ERR_ALIGN, "bl_gemv_i2s_gate_up: packed tensors must be 16-byte aligned");
   if (!aligned(x, xt == BL_F32 ? 4 : 2) || !aligned(h, ht == BL_F32 ? 4 : 2))
     return fail(BL_ERR_ALIGN, "bl_gemv_i2s_gate_up: x and h must be aligned to their element size");
-  return cuda_status(launch_gemv_i2s_gate_up(packed_gate, packed_up, x, xt, h, ht, N, K, S(stream)),
-                     "bl_gemv_i2s_gate_up");
+  return launch_status(launch_gemv_i2s_gate_up(packed_gate, packed_up, x, xt, h, ht, N, K, S(stream)),
+                       "bl_gemv_i2s_gate_up");
 }
 
 bl_status bl_gemv_tq2_0(const uint8_t* packed, const void* x, bl_dtype xt, float* y, int64_t N, int64_t K,
@@ -254,7 +264,7 @@ bl_status bl_gemv_tq2_0(const uint8_t* packed, const void* x, bl_dtype xt, float
   if (!aligned(packed, 16)) return fail(BL_ERR_ALIGN, "bl_gemv_tq2_0: packed must be 16-byte aligned");
   if (!aligned(x, xt == BL_F32 ? 4 : 2) || !aligned(y, 4))
     return fail(BL_ERR_ALIGN, "bl_gemv_tq2_0: x and y must be aligned to their element size");
-  return cuda_status(launch_gemv_tq2_0(packed, x, xt, y, N, K, S(stream)), "bl_gemv_tq2_0");
+  return launch_status(launch_gemv_tq2_0(packed, x, xt, y, N, K, S(stream)), "bl_gemv_tq2_0");
 }
 
 bl_status bl_gemm_w1a8(const int8_t* q, const float* s, const int32_t* wq, const uint16_t* ws_fp16,
@@ -273,8 +283,8 @@ bl_status bl_gemm_w1a8(const int8_t* q, const float* s, const int32_t* wq, const
   if (!aligned(q, 16) || !aligned(wq, 16) || !aligned(ws_fp16, 16) || !aligned(s, 4) || !aligned(y_bf16, 2) ||
       (bias_bf16 && !aligned(bias_bf16, 2)) || (group_dots && !aligned(group_dots, 4)))
     return fail(BL_ERR_ALIGN, "bl_gemm_w1a8: q, wq, ws must be 16-byte aligned; others to their element size");
-  return cuda_status(launch_gemm_w1a8(q, s, wq, ws_fp16, bias_bf16, M, N, K, group, y_bf16, group_dots, S(stream)),
-                     "bl_gemm_w1a8");
+  return launch_status(launch_gemm_w1a8(q, s, wq, ws_fp16, bias_bf16, M, N, K, group, y_bf16, group_dots, S(stream)),
+                       "bl_gemm_w1a8");
 }
 
 bl_status bl_gemm_w1a8_act(const void* x, bl_dtype xt, const int32_t* wq, const uint16_t* ws_fp16,
@@ -292,8 +302,8 @@ bl_status bl_gemm_w1a8_act(const void* x, bl_dtype xt, const int32_t* wq, const 
   if (!aligned(x, 16) || !aligned(wq, 16) || !aligned(ws_fp16, 16) || !aligned(y_bf16, 2) ||
       (bias_bf16 && !aligned(bias_bf16, 2)))
     return fail(BL_ERR_ALIGN, "bl_gemm_w1a8_act: x, wq, ws must be 16-byte aligned; y, bias 2-byte aligned");
-  return cuda_status(launch_gemm_w1a8_act(x, xt, wq, ws_fp16, bias_bf16, M, N, K, group, y_bf16, S(stream)),
-                     "bl_gemm_w1a8_act");
+  return launch_status(launch_gemm_w1a8_act(x, xt, wq, ws_fp16, bias_bf16, M, N, K, group, y_bf16, S(stream)),
+                       "bl_gemm_w1a8_act");
 }
 
 bl_status bl_gemm_tq2_0_int8(const int8_t* q, const float* s, const uint8_t* packed, int64_t M, int64_t N,
@@ -306,7 +316,7 @@ bl_status bl_gemm_tq2_0_int8(const int8_t* q, const float* s, const uint8_t* pac
     return fail(BL_ERR_UNSUPPORTED, "bl_gemm_tq2_0_int8: K <= 2^24 and a packed tensor under 2 GiB supported");
   if (!aligned(q, 16) || !aligned(s, 4) || !aligned(packed, 16) || !aligned(y, 16))
     return fail(BL_ERR_ALIGN, "bl_gemm_tq2_0_int8: q, packed and y must be 16-byte aligned, s 4-byte");
-  return cuda_status(launch_gemm_tq2_0_int8(q, s, packed, M, N, K, y, S(stream)), "bl_gemm_tq2_0_int8");
+  return launch_status(launch_gemm_tq2_0_int8(q, s, packed, M, N, K, y, S(stream)), "bl_gemm_tq2_0_int8");
 }
 
 bl_status bl_gemm_i2s_int8(const int8_t* q, const float* s, const uint8_t* packed, int64_t M, int64_t N, int64_t K,
@@ -318,7 +328,7 @@ bl_status bl_gemm_i2s_int8(const int8_t* q, const float* s, const uint8_t* packe
   if (K > 132096) return fail(BL_ERR_UNSUPPORTED, "bl_gemm_i2s_int8: K <= 132096 supported (K=%lld)", (long long)K);
   if (!aligned(q, 16) || !aligned(s, 16) || !aligned(packed, 16) || !aligned(y, 16) || (acc && !aligned(acc, 16)))
     return fail(BL_ERR_ALIGN, "bl_gemm_i2s_int8: all pointers must be 16-byte aligned");
-  return cuda_status(launch_gemm_i2s_int8(q, s, packed, M, N, K, y, acc, S(stream)), "bl_gemm_i2s_int8");
+  return launch_status(launch_gemm_i2s_int8(q, s, packed, M, N, K, y, acc, S(stream)), "bl_gemm_i2s_int8");
 }
 
 }  // extern "C"

@@ -13,8 +13,12 @@
  *    cudaStream_t / CUstream handle passed as void*, NULL = legacy default
  *    stream) and returns.  Nothing inside a call synchronizes with the host.
  *  - Arguments are checked on the host BEFORE any launch; a failed check
- *    returns a status and launches nothing.  A launch failure returns
- *    BL_ERR_CUDA.  bl_last_error() gives a message for the calling thread.
+ *    returns a status and launches nothing.  A shape that passes the checks
+ *    but has no launch plan (a tile, the activation records or x do not fit
+ *    in a CTA's shared memory, or a grid or tensor-map limit is exceeded)
+ *    returns BL_ERR_UNSUPPORTED, also before any launch.  A launch failure
+ *    returns BL_ERR_CUDA.  bl_last_error() gives a message for the calling
+ *    thread.
  *  - Row-major layouts throughout.  bf16 and fp16 values are passed as their
  *    16-bit patterns (uint16_t); int32 words and fp32 scales are
  *    little-endian as in device memory.
@@ -225,8 +229,11 @@ bl_status bl_gemv_i2s_gate_up(const uint8_t* packed_gate, const uint8_t* packed_
  *   packed : as written by bl_pack_tq2_0.  x : [K] fp32 or bf16.  y : fp32 [N].
  * Accuracy as for bl_gemv_i2s (fp32 output), with one fixed-point exponent
  * per 256-element block.
- * Requires K % 256 == 0, N >= 1; K <= 262144 (BL_ERR_UNSUPPORTED above);
- * `packed` 16-byte aligned, x and y aligned to their element size.
+ * Requires K % 256 == 0, N >= 1; `packed` 16-byte aligned, x and y aligned
+ * to their element size.  An 8-row tile, the activation records and x share
+ * a CTA's shared memory, which bounds K: with 227 KB per CTA (GB300), K <=
+ * 32000 for bf16 x and K <= 22528 for fp32 x; longer rows (and any K above
+ * 262144) return BL_ERR_UNSUPPORTED.
  */
 bl_status bl_gemv_tq2_0(const uint8_t* packed, const void* x, bl_dtype xt, float* y, int64_t N, int64_t K,
                         bl_stream_t stream);
