@@ -257,7 +257,10 @@ bl_status bl_gemv_tq2_0(const uint8_t* packed, const void* x, bl_dtype xt, float
  * Requires M >= 1, K % 32 == 0, group % 32 == 0, K % group == 0, N >= 1;
  * at most 1024 groups per row, and for M > 8 K <= 132096 (BL_ERR_UNSUPPORTED
  * otherwise); q, wq, ws 16-byte aligned, the other pointers aligned to
- * their element size.
+ * their element size.  For M <= 8 the tokens' activation records sit in
+ * shared memory, which bounds K further (at M = 8 about 12-16 K depending on
+ * the group size, at M = 1 from 32 K to about 100 K); longer rows return
+ * BL_ERR_UNSUPPORTED.
  */
 bl_status bl_gemm_w1a8(const int8_t* q, const float* s, const int32_t* wq, const uint16_t* ws_fp16,
                        const uint16_t* bias_bf16, int64_t M, int64_t N, int64_t K, int group, uint16_t* y_bf16,
