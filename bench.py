@@ -333,6 +333,12 @@ def bench_ours(args, dist):
     extra = {}
     if not args.no_extra:
         extra = bench_secondary(args, B, torch, stream, dist, hbm, bf16_burst)
+        try:  # a reported extra: it never stops the headline line
+            extra["cold_single_launch_mlp"] = cold_launches(
+                torch, stream, {"mlp_step": mlp_step, "gate_up": gate_up_only,
+                                "down": lambda i: B.bl_gemv_i2s(mats["down"][i % COPIES], yg, 2560, 6912, y=ydn)})
+        except Exception as e:  # noqa: BLE001
+            extra["cold_single_launch_mlp"] = {"error": repr(e)[:200]}
     del mats
     torch.cuda.empty_cache()
 
@@ -366,6 +372,32 @@ def bench_ours(args, dist):
             "secondary": extra,
         }
         print(json.dumps(line))
+
+
+def cold_launches(torch, stream, calls, reps=50):
+    """Median time of one call with L2 flushed before it (a buffer of twice the L2
+    size is written between calls), for each named call; microseconds."""
+    props = torch.cuda.get_device_properties(torch.cuda.current_device())
+    l2 = int(getattr(props, "L2_cache_size", 0) or (129 << 20))
+    flush = torch.empty(2 * l2 // 4, dtype=torch.float32, device="cuda")
+    out = {}
+    with torch.cuda.stream(stream):
+        for name, fn in calls.items():
+            ts = []
+            for i in range(reps + 3):
+                flush.zero_()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                fn(i)
+                e1.record(stream)
+                e1.synchronize()
+                if i >= 3:
+                    ts.append(e0.elapsed_time(e1) * 1e3)
+            out[name + "_us"] = round(float(np.median(ts)), 3)
+    torch.cuda.synchronize()
+    del flush
+    out["how"] = "median of %d single calls, each after writing %d MB (2x L2)" % (reps, 2 * l2 >> 20)
+    return out
 
 
 def bench_secondary(args, B, torch, stream, dist, hbm, bf16_peak):
