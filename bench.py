@@ -600,9 +600,23 @@ def cpu_baseline(seconds):
         o.step()
         n += 1
     dt = time.perf_counter() - t0
-    return {"value": round(o.bytes_per_step * n / dt / 1e9, 4), "unit": UNIT, "cores": o.cores if o.O.has_openmp() else 1,
-            "kind": "oracle",
-            "sample": "%d full MLP steps (fused gate/up then down, all rows, one token) in %.1f s" % (n, dt)}
+    out = {"value": round(o.bytes_per_step * n / dt / 1e9, 4), "unit": UNIT, "cores": o.cores if o.O.has_openmp() else 1,
+           "kind": "oracle",
+           "sample": "%d full MLP steps (fused gate/up then down, all rows, one token) in %.1f s" % (n, dt)}
+    # the same oracle on one host thread, for a quarter of the time
+    o.O.set_threads(1)
+    try:
+        t0 = time.perf_counter()
+        n1 = 0
+        while n1 == 0 or time.perf_counter() - t0 < seconds / 4:
+            o.step()
+            n1 += 1
+        dt1 = time.perf_counter() - t0
+    finally:
+        o.O.set_threads(o.cores)
+    out["one_thread"] = {"value": round(o.bytes_per_step * n1 / dt1 / 1e9, 4), "unit": UNIT, "cores": 1,
+                         "sample": "%d full MLP steps in %.1f s" % (n1, dt1)}
+    return out
 
 
 def bench_reference(args, dist):
