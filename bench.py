@@ -339,6 +339,14 @@ def bench_ours(args, dist):
                                 "down": lambda i: B.bl_gemv_i2s(mats["down"][i % COPIES], yg, 2560, 6912, y=ydn)})
         except Exception as e:  # noqa: BLE001
             extra["cold_single_launch_mlp"] = {"error": repr(e)[:200]}
+        try:  # the int8 products against the legacy integer MMA's measured rate as well
+            pk = mma_s8_peak(torch, B, stream)
+            extra["mma_sync_s8_peak"] = pk
+            for k, v in extra.items():
+                if isinstance(v, dict) and v.get("unit") == "TOPS (int8 ops)":
+                    v["frac_mma_sync_s8_peak"] = round(v["value"] / pk["tops"], 4)
+        except Exception as e:  # noqa: BLE001
+            extra["mma_sync_s8_peak"] = {"error": repr(e)[:200]}
     del mats
     torch.cuda.empty_cache()
 
@@ -398,6 +406,31 @@ def cold_launches(torch, stream, calls, reps=50):
     del flush
     out["how"] = "median of %d single calls, each after writing %d MB (2x L2)" % (reps, 2 * l2 >> 20)
     return out
+
+
+def mma_s8_peak(torch, B, stream, iters=2048, reps=5):
+    """Measured rate of the warp-level int8 MMA (bl_probe_mma_s8), the legacy
+    integer tensor path: a second denominator for the int8 products."""
+    L = B.lib()
+    props = torch.cuda.get_device_properties(torch.cuda.current_device())
+    scratch = torch.empty(props.multi_processor_count * 16 * 256, dtype=torch.int32, device="cuda")
+    ops = ctypes.c_int64(0)
+    args = (ctypes.c_void_p(scratch.data_ptr()), scratch.numel(), iters, ctypes.byref(ops),
+            ctypes.c_void_p(stream.cuda_stream))
+    with torch.cuda.stream(stream):
+        bad = L.bl_probe_mma_s8(*args)  # warm-up
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            bad |= L.bl_probe_mma_s8(*args)
+        e1.record(stream)
+        torch.cuda.synchronize()
+    if bad:
+        raise RuntimeError("bl_probe_mma_s8: " + L.bl_last_error().decode())
+    ms = e0.elapsed_time(e1) / reps
+    return {"tops": round(ops.value / (ms * 1e-3) / 1e12, 1), "us_per_launch": round(ms * 1e3, 2),
+            "how": "mma.sync m16n8k32 s8, register-only, all SMs; mean of %d launches" % reps}
 
 
 def bench_secondary(args, B, torch, stream, dist, hbm, bf16_peak):
