@@ -334,7 +334,7 @@ bl_status bl_gemm_i2s_int8(const int8_t* q, const float* s, const uint8_t* packe
   if (M < 1 || N < 1 || K < 128 || K % 128 || N > 0x7fffffff || M > 0x7fffffff)
     return fail(BL_ERR_SHAPE, "bl_gemm_i2s_int8: need M, N >= 1, K %% 128 == 0 (M=%lld N=%lld K=%lld)", (long long)M,
                 (long long)N, (long long)K);
-  if (K > 132096) return fail(BL_ERR_UNSUPPORTED, "bl_gemm_i2s_int8: K <= 132096 supported (K=%lld)", (long long)K);
+  if (K > 131072) return fail(BL_ERR_UNSUPPORTED, "bl_gemm_i2s_int8: K <= 131072 supported (K=%lld)", (long long)K);
   if (!aligned(q, 16) || !aligned(s, 16) || !aligned(packed, 16) || !aligned(y, 16) || (acc && !aligned(acc, 16)))
     return fail(BL_ERR_ALIGN, "bl_gemm_i2s_int8: all pointers must be 16-byte aligned");
   return launch_status(launch_gemm_i2s_int8(q, s, packed, M, N, K, y, acc, S(stream)), "bl_gemm_i2s_int8");

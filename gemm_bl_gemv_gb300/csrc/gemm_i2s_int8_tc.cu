@@ -7,7 +7,7 @@
 // Exactness.  The MMA runs kind::f16 (fp16 operands, fp32 accumulation).
 // Activations and weights enter as power-of-two multiples of q and w whose
 // products are exactly q*w (see "Scaled operands" below); every partial sum
-// is an integer of magnitude <= K * 127 < 2^24 (K <= 132096), so the fp32
+// is an integer of magnitude <= K * 128 <= 2^24 (K <= 131072), so the fp32
 // accumulator holds the exact integer sum.  (This toolchain does not accept
 // tcgen05 .kind::i8 for sm_103a.)
 //

@@ -323,8 +323,9 @@ bl_status bl_gemm_tq2_0_int8(const int8_t* q, const float* s, const uint8_t* pac
  *   y[m,n]   = f32(acc[m,n]) * s[m] * scale  (scale: the i2_s tensor scale)
  *   q : int8 [M, K];  s : fp32 [M];  packed : i2_s tensor (bl_pack_i2s).
  *   y : fp32 [M, N];  acc : int32 [M, N] or NULL (when given, also written).
- * Requires M >= 1, N >= 1, K % 128 == 0, K <= 132096 (so that every
- * accumulator stays exactly representable); all pointers 16-byte aligned.
+ * Requires M >= 1, N >= 1, K % 128 == 0, K <= 131072 (then |acc| <= 128 K
+ * <= 2^24 for any int8 q, so every partial sum stays exactly representable
+ * in the fp32 tensor-core accumulator); all pointers 16-byte aligned.
  */
 bl_status bl_gemm_i2s_int8(const int8_t* q, const float* s, const uint8_t* packed, int64_t M, int64_t N, int64_t K,
                            float* y, int32_t* acc, bl_stream_t stream);

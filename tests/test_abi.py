@@ -168,6 +168,7 @@ def test_every_documented_rejection_without_gpu():
         (L.bl_gemm_tq2_0_int8, (a, o2, a, 4, 4, 256, a, None), AL),
         (L.bl_gemm_tq2_0_int8, (a, a, a, 4, 4, 256, o4, None), AL),
         (L.bl_gemm_i2s_int8, (a, a, None, 4, 4, 128, a, None, None), NULL),
+        (L.bl_gemm_i2s_int8, (a, a, a, 64, 4, 131072 + 128, a, None, None), UN),  # 128 K > 2^24
         (L.bl_gemm_i2s_int8, (a, a, a, 4, 0, 128, a, None, None), ERR),
         (L.bl_gemm_i2s_int8, (a, a, a, 4, 4, 192, a, None, None), ERR),
         (L.bl_gemm_i2s_int8, (a, o4, a, 4, 4, 128, a, None, None), AL),
