@@ -186,7 +186,7 @@ bl_status bl_quantize_act_absmax_int8(const void* x, bl_dtype xt, int64_t M, int
  * Accuracy: within each 128-element group x is carried as a fixed-point
  * integer of 30 bits (fp32 input), 22 bits (bf16 input, fp32 output) or 14
  * bits (bf16 input and output) relative to the group's max|x|: values
- * within 6, 14 or 6 binades of the group maximum (respectively) are carried
+ * within 7, 15 or 7 binades of the group maximum (respectively) are carried
  * exactly, smaller values with an absolute error of at most 2^-31, 2^-23 or
  * 2^-15 times the group maximum (the last far below the 2^-9 relative
  * rounding of a bf16 output).  Products and sums inside a group are exact integers; each group

@@ -148,3 +148,19 @@ def test_gemv_digit_decomposition():
         codes = g.integers(0, 3, X.size)                     # c = w + 1
         dots = sum((codes * digits[d]).sum() * 256 ** d for d in range(D - 1)) + (codes * top).sum() * 256 ** (D - 1)
         assert dots - X.sum() == ((codes - 1) * X).sum()
+
+
+def test_gemv_fixed_point_exact_range():
+    """The GEMV fixed point: with the group maximum m in [2^(e-1), 2^e) and
+    F = (8D - 1) - e, x * 2^F is an integer of magnitude < 2^(8D-1) for every
+    |x| <= m whose binade is at most (8D - 1) - p below m's (p: significand
+    bits, 24 for fp32 and 8 for bf16): 7, 15 and 7 binades for
+    (fp32, D=4), (bf16, D=3) and (bf16, D=2); one binade lower it is not."""
+    for p, D, span in ((24, 4, 7), (8, 3, 15), (8, 2, 7)):
+        e = 1                                            # m in [1, 2)
+        F = (8 * D - 1) - e
+        top = (2 ** p - 1) / 2 ** (p - 1)                # largest significand, the group maximum
+        assert top * 2.0 ** F < 2 ** (8 * D - 1)
+        odd = 1 + 2.0 ** (1 - p)                         # significand with its lowest bit set
+        assert float(odd * 2.0 ** (-span) * 2.0 ** F).is_integer()
+        assert not float(odd * 2.0 ** (-span - 1) * 2.0 ** F).is_integer()
