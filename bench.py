@@ -347,6 +347,10 @@ def bench_ours(args, dist):
                     v["frac_mma_sync_s8_peak"] = round(v["value"] / pk["tops"], 4)
         except Exception as e:  # noqa: BLE001
             extra["mma_sync_s8_peak"] = {"error": repr(e)[:200]}
+        try:
+            extra["act_quant_bf16"] = act_quant_times(torch, B, stream, hbm)
+        except Exception as e:  # noqa: BLE001
+            extra["act_quant_bf16"] = {"error": repr(e)[:200]}
     del mats
     torch.cuda.empty_cache()
 
@@ -431,6 +435,38 @@ def mma_s8_peak(torch, B, stream, iters=2048, reps=5):
     ms = e0.elapsed_time(e1) / reps
     return {"tops": round(ops.value / (ms * 1e-3) / 1e12, 1), "us_per_launch": round(ms * 1e3, 2),
             "how": "mma.sync m16n8k32 s8, register-only, all SMs; mean of %d launches" % reps}
+
+
+def act_quant_times(torch, B, stream, hbm, shapes=((512, 2560), (8, 5120)), reps=200):
+    """The per-token act-quant launch alone (bf16 x), eager back-to-back
+    launches timed with events: microseconds and GB/s of x read plus q and s
+    written."""
+    L = B.lib()
+    out = {}
+    vp = ctypes.c_void_p
+    for M, K in shapes:
+        xb = synth.activations(WL.index, M, K, "bf16")
+        x = torch.from_numpy(xb.view(np.int16)).cuda().view(torch.bfloat16)
+        q = torch.empty((M, K), dtype=torch.int8, device="cuda")
+        sc = torch.empty(M, dtype=torch.float32, device="cuda")
+        args = (vp(x.data_ptr()), B.BL_BF16, M, K, vp(q.data_ptr()), vp(sc.data_ptr()), vp(stream.cuda_stream))
+        with torch.cuda.stream(stream):
+            bad = 0
+            for _ in range(10):
+                bad |= L.bl_quantize_act_absmax_int8(*args)
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(reps):
+                bad |= L.bl_quantize_act_absmax_int8(*args)
+            e1.record(stream)
+            torch.cuda.synchronize()
+        if bad:
+            raise RuntimeError("bl_quantize_act_absmax_int8: " + L.bl_last_error().decode())
+        us = e0.elapsed_time(e1) * 1e3 / reps
+        gbs = (2 * M * K + M * K + 4 * M) / (us * 1e-6) / 1e9
+        out["M%d_K%d" % (M, K)] = {"us_per_launch": round(us, 3), "GBps": round(gbs, 1), "frac_hbm": round(gbs / hbm, 4)}
+    return out
 
 
 def bench_secondary(args, B, torch, stream, dist, hbm, bf16_peak):
