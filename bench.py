@@ -22,6 +22,7 @@ i2_s int8 prefill at M=512 in TOPS).
 a bounded sample of the same workload and prints the same JSON line.
 """
 import argparse
+import contextlib
 import ctypes
 import hashlib
 import json
@@ -184,6 +185,21 @@ def upload_i2s(B, torch, wl_index, tensor, N, K, p_zero, scale, copies):
     return [packed] + [packed.clone() for _ in range(copies - 1)]
 
 
+@contextlib.contextmanager
+def nvtx(torch, name):
+    """An NVTX range for profilers (ncu --nvtx); nothing when NVTX is unavailable."""
+    try:
+        torch.cuda.nvtx.range_push(name)
+        pushed = True
+    except Exception:  # noqa: BLE001
+        pushed = False
+    try:
+        yield
+    finally:
+        if pushed:
+            torch.cuda.nvtx.range_pop()
+
+
 def time_graph(torch, dist, body, steps, warmup, graph_steps, stream):
     """Capture `graph_steps` steps in a graph, replay: warm-up, then exactly `steps` timed steps."""
     assert steps % graph_steps == 0 and warmup % graph_steps == 0
@@ -270,7 +286,7 @@ def bench_ours(args, dist):
         B.bl_gemv_i2s(mats["down"][c], yg, 2560, 6912, y=ydn)
 
     gs = args.graph_steps
-    with ClockSampler(torch.cuda.current_device()) as clk:
+    with ClockSampler(torch.cuda.current_device()) as clk, nvtx(torch, "mlp_step_timed"):
         ms = time_graph(torch, dist, mlp_step, args.steps, args.warmup, gs, stream)
     ms = dist.max(ms)
     step_bytes = mlp_bytes()
@@ -283,7 +299,8 @@ def bench_ours(args, dist):
         B.bl_gemv_i2s_gate_up(mats["gate"][c], mats["up"][c], x, 6912, 2560, h=yg)
 
     gu_steps = max(gs, (min(args.steps, 20000) // gs) * gs)
-    gu_ms = dist.max(time_graph(torch, dist, gate_up_only, gu_steps, gs, gs, stream))
+    with nvtx(torch, "gate_up_alone"):
+        gu_ms = dist.max(time_graph(torch, dist, gate_up_only, gu_steps, gs, gs, stream))
     avg_launch_s = gu_ms * 1e-3 / gu_steps
     achieved = gate_up_algorithmic_bytes() / avg_launch_s / 1e9
 
@@ -332,7 +349,8 @@ def bench_ours(args, dist):
 
     extra = {}
     if not args.no_extra:
-        extra = bench_secondary(args, B, torch, stream, dist, hbm, bf16_burst)
+        with nvtx(torch, "secondary"):
+            extra = bench_secondary(args, B, torch, stream, dist, hbm, bf16_burst)
         try:  # a reported extra: it never stops the headline line
             extra["cold_single_launch_mlp"] = cold_launches(
                 torch, stream, {"mlp_step": mlp_step, "gate_up": gate_up_only,
