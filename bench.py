@@ -369,6 +369,10 @@ def bench_ours(args, dist):
             extra["act_quant_bf16"] = act_quant_times(torch, B, stream, hbm)
         except Exception as e:  # noqa: BLE001
             extra["act_quant_bf16"] = {"error": repr(e)[:200]}
+        try:
+            extra["e2e_graph_replay"] = e2e_graph_replay(torch, stream, e2e_step, step_bytes)
+        except Exception as e:  # noqa: BLE001
+            extra["e2e_graph_replay"] = {"error": repr(e)[:200]}
     del mats
     torch.cuda.empty_cache()
 
@@ -402,6 +406,35 @@ def bench_ours(args, dist):
             "secondary": extra,
         }
         print(json.dumps(line))
+
+
+def e2e_graph_replay(torch, stream, step, step_bytes, steps=2000, graph_steps=100):
+    """The e2e step (pinned host x in, both products, y back to pinned host)
+    through the same C-ABI calls, captured once in a CUDA graph of
+    `graph_steps` steps and replayed: what a serving loop built on graphs pays
+    per step.  Reported beside the eager e2e figure, not in its place."""
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        bad = 0
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(graph_steps):
+                bad |= step(i)
+        if bad:
+            raise RuntimeError("a C ABI call or copy failed during capture")
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps // graph_steps):
+            g.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1)
+    n = (steps // graph_steps) * graph_steps
+    return {"value": round(step_bytes * n / (ms * 1e-3) / 1e9, 2), "unit": UNIT,
+            "us_per_step": round(ms * 1e3 / n, 3),
+            "how": "C ABI calls and both copies captured in a CUDA graph of %d steps, %d steps replayed" % (graph_steps, n)}
 
 
 def cold_launches(torch, stream, calls, reps=50):
