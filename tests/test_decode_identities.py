@@ -164,3 +164,49 @@ def test_gemv_fixed_point_exact_range():
         odd = 1 + 2.0 ** (1 - p)                         # significand with its lowest bit set
         assert float(odd * 2.0 ** (-span) * 2.0 ** F).is_integer()
         assert not float(odd * 2.0 ** (-span - 1) * 2.0 ** F).is_integer()
+
+
+def test_i2s_gemv_shift_class_masks():
+    """i2_s GEMV decode: in a 32-bit word holding bytes p..p+3 of a group, the
+    four masks w & 0x03030303, (w >> 2) & 0x03030303, w & 0x30303030 and
+    (w >> 2) & 0x30303030 hold, byte by byte, the codes of elements 96+p,
+    64+p (times 1) and 32+p, p (times 16): shift 0, 2, 4, 6 of each byte."""
+    g = np.random.Generator(np.random.PCG64(53))
+    words = g.integers(0, 2 ** 32, 2000, dtype=np.uint64)
+    for w in words:
+        w = int(w)
+        byts = [(w >> (8 * b)) & 0xFF for b in range(4)]
+        masks = [w & 0x03030303, (w >> 2) & 0x03030303, w & 0x30303030, (w >> 2) & 0x30303030]
+        scale = [1, 1, 16, 16]
+        shift = [0, 2, 4, 6]
+        for mk, sc, sh in zip(masks, scale, shift):
+            for b in range(4):
+                assert ((mk >> (8 * b)) & 0xFF) == sc * ((byts[b] >> sh) & 3)
+
+
+def test_w1_bit_class_masks():
+    """W1A8 rows decode: word & (0x01010101 << j) holds, in byte b, bit j of
+    byte b times 2^j, i.e. element 8b + j of the 32-element word; so the eight
+    class sums acc_j = 2^j S_j recombine as sum_j acc_j >> j."""
+    g = np.random.Generator(np.random.PCG64(59))
+    for w in g.integers(0, 2 ** 32, 500, dtype=np.uint64):
+        w = int(w)
+        a = g.integers(-128, 128, 32)
+        S = 0
+        for j in range(8):
+            m = w & (0x01010101 << j)
+            acc = sum(((m >> (8 * b)) & 0xFF) * a[8 * b + j] for b in range(4))
+            assert acc % (1 << j) == 0
+            S += acc >> j
+        bits = [(w >> k) & 1 for k in range(32)]
+        assert S == sum(int(a[k]) for k in range(32) if bits[k])
+
+
+def test_block_scales_include_subnormals():
+    """The |N(0, 0.02)| fp16 block and group scales of the workloads include
+    fp16 subnormals (about 0.24% of them), so the exact subnormal decode of
+    every scale path is exercised by the parity inputs."""
+    from gemm_bl_gemv_gb300 import synth
+    d = synth.block_scale_matrix(3, 2048, 20)
+    sub = np.mean((d & 0x7C00) == 0)
+    assert 0.001 < sub < 0.005
