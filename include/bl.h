@@ -188,12 +188,13 @@ bl_status bl_quantize_act_absmax_int8(const void* x, bl_dtype xt, int64_t M, int
  * bits (bf16 input and output) relative to the group's max|x|: values
  * within 7, 15 or 7 binades of the group maximum (respectively) are carried
  * exactly, smaller values with an absolute error of at most 2^-31, 2^-23 or
- * 2^-15 times the group maximum (the last far below the 2^-9 relative
- * rounding of a bf16 output).  Products and sums inside a group are exact integers; each group
- * sum is converted to fp32 once and the group sums are added in fp32, then
- * rounded to bf16 if asked.  For activations without extreme in-group
- * outliers the error is within 1e-5 (fp32 output) / 2e-2 (bf16 output) of
- * |scale| * sum_j |w[i,j]| |x[j]| + |y[i]|.
+ * 2^-15 times the group maximum.  Products and sums inside a group are exact
+ * integers; the partial sums are converted to fp32 once each and added in
+ * fp32, then rounded to bf16 if asked.  The error of y[i] is at most
+ * rho |y[i]| + 1e-5 |scale| sum_j |w[i,j]| |x[j]| (rho = 1e-5 for fp32 output,
+ * 2^-7 for bf16 output: twice its rounding), plus, for activations outside
+ * the exact range, |scale| sum_g E max|x_g| sum_{j in g} |w[i,j]| with
+ * E = 2^-31, 2^-23 or 2^-15 as above.
  * Requires K % 128 == 0, K <= 32768, N >= 1; `packed` 16-byte aligned; x
  * and y aligned to their element size.  Non-finite x gives unspecified y.
  */
