@@ -66,6 +66,21 @@ def mlp_bytes():
     return sum(packed_bytes(*WL.extra[m]) for m in MATS)
 
 
+DTYPE = "bf16 io; s16 fixed point x ternary codes -> s32"
+ARITH = ("bf16 x and h and y; per 128-element group x is carried as 16-bit fixed point (two byte digits) and "
+         "dotted with the 2-bit codes by dp4a into exact int32 sums; fp32 epilogue")
+
+
+def headline_config(world):
+    """The workload both arms time (the same dict in both JSON lines)."""
+    return {"workload": WL.name, "model": "BitNet-2B-shaped MLP (random ternary weights)",
+            "global_batch": 1, "seq_len": 1, "parallelism": "replicas" if world > 1 else "single",
+            "M": 1, "shapes_NxK": [list(WL.extra[m]) for m in MATS], "x": "bf16", "y": "bf16",
+            "step": "h = relu(W_gate x)^2 * (W_up x) [one fused launch]; y = W_down h",
+            "l2": "GPU arm: inputs larger than L2 (%d rotating weight copies, %d MB); CPU reference arm: one copy"
+                  % (COPIES, COPIES * mlp_bytes() >> 20)}
+
+
 def gate_up_algorithmic_bytes():
     """Per fused gate/up launch: both packed tensors (scales included) + x (bf16) + h (bf16)."""
     N, K = WL.extra["gate"]
@@ -200,9 +215,25 @@ def nvtx(torch, name):
             torch.cuda.nvtx.range_pop()
 
 
+def graph_size(steps, cap):
+    """The largest divisor of `steps` that is at most `cap`: a graph of that
+    many steps, replayed, times exactly `steps` steps."""
+    for g in range(min(cap, steps), 0, -1):
+        if steps % g == 0:
+            return g
+    return 1
+
+
+def warm_steps(warmup, graph_steps):
+    """Warm-up in whole graph replays: at least `warmup` steps (and at least 3), at least one replay."""
+    return max(1, -(-max(3, warmup) // graph_steps)) * graph_steps
+
+
 def time_graph(torch, dist, body, steps, warmup, graph_steps, stream):
-    """Capture `graph_steps` steps in a graph, replay: warm-up, then exactly `steps` timed steps."""
-    assert steps % graph_steps == 0 and warmup % graph_steps == 0
+    """Capture `graph_steps` steps in a graph, replay: warm-up (whole replays
+    covering at least `warmup` steps), then exactly `steps` timed steps."""
+    assert steps % graph_steps == 0
+    warmup = warm_steps(warmup, graph_steps)
     g = torch.cuda.CUDAGraph()
     with torch.cuda.stream(stream):
         for i in range(2):  # eager warm-up (kernel attributes, lazy loading)
@@ -285,7 +316,7 @@ def bench_ours(args, dist):
         B.bl_gemv_i2s_gate_up(mats["gate"][c], mats["up"][c], x, 6912, 2560, h=yg)
         B.bl_gemv_i2s(mats["down"][c], yg, 2560, 6912, y=ydn)
 
-    gs = args.graph_steps
+    gs = graph_size(args.steps, args.graph_steps)
     with ClockSampler(torch.cuda.current_device()) as clk, nvtx(torch, "mlp_step_timed"):
         ms = time_graph(torch, dist, mlp_step, args.steps, args.warmup, gs, stream)
     ms = dist.max(ms)
@@ -298,9 +329,10 @@ def bench_ours(args, dist):
         c = i % COPIES
         B.bl_gemv_i2s_gate_up(mats["gate"][c], mats["up"][c], x, 6912, 2560, h=yg)
 
-    gu_steps = max(gs, (min(args.steps, 20000) // gs) * gs)
+    gu_steps = args.roofline_launches
+    gu_gs = graph_size(gu_steps, 1000)
     with nvtx(torch, "gate_up_alone"):
-        gu_ms = dist.max(time_graph(torch, dist, gate_up_only, gu_steps, gs, gs, stream))
+        gu_ms = dist.max(time_graph(torch, dist, gate_up_only, gu_steps, 2 * gu_gs, gu_gs, stream))
     avg_launch_s = gu_ms * 1e-3 / gu_steps
     achieved = gate_up_algorithmic_bytes() / avg_launch_s / 1e9
 
@@ -357,14 +389,6 @@ def bench_ours(args, dist):
                                 "down": lambda i: B.bl_gemv_i2s(mats["down"][i % COPIES], yg, 2560, 6912, y=ydn)})
         except Exception as e:  # noqa: BLE001
             extra["cold_single_launch_mlp"] = {"error": repr(e)[:200]}
-        try:  # the int8 products against the legacy integer MMA's measured rate as well
-            pk = mma_s8_peak(torch, B, stream)
-            extra["mma_sync_s8_peak"] = pk
-            for k, v in extra.items():
-                if isinstance(v, dict) and v.get("unit") == "TOPS (int8 ops)":
-                    v["frac_mma_sync_s8_peak"] = round(v["value"] / pk["tops"], 4)
-        except Exception as e:  # noqa: BLE001
-            extra["mma_sync_s8_peak"] = {"error": repr(e)[:200]}
         try:
             extra["act_quant_bf16"] = act_quant_times(torch, B, stream, hbm)
         except Exception as e:  # noqa: BLE001
@@ -384,19 +408,15 @@ def bench_ours(args, dist):
         line = {
             "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": dist.world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "int32",
-            "arith": "dp4a int32 dots of per-group 16-bit fixed-point activation digits and ternary codes; fp32 epilogue", "data": "synthetic",
-            "config": {"workload": WL.name, "model": "BitNet-2B-shaped MLP (random ternary weights)",
-                       "global_batch": 1, "seq_len": 1, "parallelism": "replicas" if dist.world > 1 else "single",
-                       "M": 1, "shapes_NxK": [list(WL.extra[m]) for m in MATS], "x": "bf16", "y": "bf16",
-                       "step": "h = relu(W_gate x)^2 * (W_up x) [one fused launch]; y = W_down h",
-                       "weight_copies": COPIES, "l2": "inputs larger than L2 (24 rotating weight copies, 320 MB)",
-                       "launch": "CUDA graph of %d steps, programmatic dependent launch" % gs},
+            "vs_baseline": None, "dtype": DTYPE, "arith": ARITH, "data": "synthetic",
+            "config": headline_config(dist.world),
+            "launch": "CUDA graph of %d steps replayed %d times, programmatic dependent launch; warm-up %d steps "
+                      "(whole replays)" % (gs, args.steps // gs, warm_steps(args.warmup, gs)),
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
                          "frac": round(achieved / hbm, 4), "traffic": profiled_traffic(),
                          "kernel": "gemv_i2s_kernel<D=2, bf16 x, bf16 y, gate+up>",
                          "algorithmic_bytes_per_launch": gate_up_algorithmic_bytes(),
-                         "avg_launch_us": round(avg_launch_s * 1e6, 3),
+                         "avg_launch_us": round(avg_launch_s * 1e6, 3), "launches_timed": gu_steps,
                          "peak_source": peak_src + " copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"},
             "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "steps": e2e_steps, "api": "C ABI (bl_gemv_i2s_gate_up, bl_gemv_i2s) per step with cudaMemcpyAsync from/to pinned host memory, eager"},
@@ -461,31 +481,6 @@ def cold_launches(torch, stream, calls, reps=50):
     del flush
     out["how"] = "median of %d single calls, each after writing %d MB (2x L2)" % (reps, 2 * l2 >> 20)
     return out
-
-
-def mma_s8_peak(torch, B, stream, iters=2048, reps=5):
-    """Measured rate of the warp-level int8 MMA (bl_probe_mma_s8), the legacy
-    integer tensor path: a second denominator for the int8 products."""
-    L = B.lib()
-    props = torch.cuda.get_device_properties(torch.cuda.current_device())
-    scratch = torch.empty(props.multi_processor_count * 16 * 256, dtype=torch.int32, device="cuda")
-    ops = ctypes.c_int64(0)
-    args = (ctypes.c_void_p(scratch.data_ptr()), scratch.numel(), iters, ctypes.byref(ops),
-            ctypes.c_void_p(stream.cuda_stream))
-    with torch.cuda.stream(stream):
-        bad = L.bl_probe_mma_s8(*args)  # warm-up
-        torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(reps):
-            bad |= L.bl_probe_mma_s8(*args)
-        e1.record(stream)
-        torch.cuda.synchronize()
-    if bad:
-        raise RuntimeError("bl_probe_mma_s8: " + L.bl_last_error().decode())
-    ms = e0.elapsed_time(e1) / reps
-    return {"tops": round(ops.value / (ms * 1e-3) / 1e12, 1), "us_per_launch": round(ms * 1e3, 2),
-            "how": "mma.sync m16n8k32 s8, register-only, all SMs; mean of %d launches" % reps}
 
 
 def act_quant_times(torch, B, stream, hbm, shapes=((512, 2560), (8, 5120)), reps=200):
@@ -761,9 +756,9 @@ def bench_reference(args, dist):
     line = {
         "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": dist.world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f64 (oracle)", "data": "synthetic", "impl": "reference",
-        "config": {"workload": WL.name, "model": "BitNet-2B-shaped MLP (random ternary weights)", "global_batch": 1,
-                   "seq_len": 1, "parallelism": "single", "M": 1},
+        "vs_baseline": None, "dtype": "f64 (oracle)", "arith": "fp64 accumulation of the decoded ternary weights times x",
+        "data": "synthetic", "impl": "reference",
+        "config": headline_config(dist.world),
         "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
                          "sample": "each step: the MLP on %.4f of each matrix's rows" % frac},
         "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -777,7 +772,9 @@ def main():
     ap.add_argument("--steps", type=int, default=200000)
     ap.add_argument("--warmup", type=int, default=4000)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--graph-steps", type=int, default=1000)
+    ap.add_argument("--graph-steps", type=int, default=1000, help="most steps captured in one graph")
+    ap.add_argument("--roofline-launches", type=int, default=20000,
+                    help="back-to-back launches of the dominant kernel timed for the roofline object")
     ap.add_argument("--e2e-steps", type=int, default=20000)
     ap.add_argument("--secondary-steps", type=int, default=2000)
     ap.add_argument("--no-extra", action="store_true")
@@ -790,12 +787,6 @@ def main():
         if args.impl == "reference":
             bench_reference(args, dist)
         else:
-            gs = min(args.graph_steps, args.steps)
-            while args.steps % gs or args.warmup % gs:
-                gs -= 1
-            args.graph_steps = gs
-            if args.warmup < 3:
-                args.warmup = 3 * gs if 3 * gs >= 3 else 3
             bench_ours(args, dist)
     finally:
         dist.close()

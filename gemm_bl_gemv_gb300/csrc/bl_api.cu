@@ -156,15 +156,6 @@ bl_status bl_device_error(uint32_t* flags, int clear) {
 void bl_set_overlap(int enable) { g_overlap.store(enable ? 1 : 0); }
 int bl_get_overlap(void) { return g_overlap.load(); }
 
-bl_status bl_probe_mma_s8(int32_t* scratch, int64_t scratch_len, int iters, int64_t* ops, bl_stream_t stream) {
-  if (!scratch || !ops) return fail(BL_ERR_NULL, "bl_probe_mma_s8: NULL pointer");
-  if (scratch_len < 256 || iters < 1)
-    return fail(BL_ERR_SHAPE, "bl_probe_mma_s8: need scratch_len >= 256 and iters >= 1 (scratch_len=%lld iters=%d)",
-                (long long)scratch_len, iters);
-  if (!aligned(scratch, 4)) return fail(BL_ERR_ALIGN, "bl_probe_mma_s8: scratch must be 4-byte aligned");
-  return cuda_status(launch_mma_s8_probe(iters, scratch, scratch_len, ops, S(stream)), "bl_probe_mma_s8");
-}
-
 bl_status bl_pack_i2s(const int8_t* w, float scale, int64_t N, int64_t K, uint8_t* out, bl_stream_t stream) {
   if (!w || !out) return fail(BL_ERR_NULL, "bl_pack_i2s: NULL pointer");
   if (N < 1 || K < 128 || K % 128) return fail(BL_ERR_SHAPE, "bl_pack_i2s: need N >= 1, K %% 128 == 0 (N=%lld K=%lld)",

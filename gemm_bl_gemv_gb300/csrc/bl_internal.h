@@ -124,7 +124,6 @@ cudaError_t launch_gemm_tq2_0_int8(const int8_t* q, const float* s, const uint8_
                                    int64_t K, float* y, cudaStream_t st);
 // Warp-level int8 MMA throughput probe: enqueues the kernel on `s` and sets
 // *ops to the integer operations it performs (out: out_len ints of scratch).
-cudaError_t launch_mma_s8_probe(int iters, int32_t* out, int64_t out_len, int64_t* ops, cudaStream_t s);
 cudaError_t launch_gemm_i2s_int8_simt(const int8_t* q, const float* sc, const uint8_t* packed, int64_t M, int64_t N,
                                       int64_t K, float* y, int32_t* acc, cudaStream_t s);
 cudaError_t launch_gemm_i2s_int8(const int8_t* q, const float* sc, const uint8_t* packed, int64_t M, int64_t N,

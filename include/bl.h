@@ -91,21 +91,6 @@ bl_status bl_device_error(uint32_t* flags, int clear);
 void bl_set_overlap(int enable);
 int bl_get_overlap(void);
 
-/*
- * Measurement aid, not a product: enqueue a throughput probe of the
- * warp-level int8 MMA (mma.sync m16n8k32, s8 x s8 -> s32) on `stream`, the
- * legacy integer tensor path, as a second denominator for the int8
- * products (which run exactly on the tcgen05 fp16 pipe).  The caller times
- * it with events.
- *   scratch : int32 [scratch_len] device buffer; one int per probe thread is
- *             written (the grid is capped at scratch_len / 256 CTAs).
- *   iters   : loop trips per warp (each trip is four MMAs), >= 1.
- *   ops     : host pointer; receives the integer operations (2*M*N*K per MMA)
- *             the launch performs.
- * Requires scratch_len >= 256, scratch 4-byte aligned.
- */
-bl_status bl_probe_mma_s8(int32_t* scratch, int64_t scratch_len, int iters, int64_t* ops, bl_stream_t stream);
-
 /* ------------------------------------------------------------------------ */
 /* Packing (load time).                                                       */
 /* ------------------------------------------------------------------------ */

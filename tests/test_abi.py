@@ -104,13 +104,8 @@ def test_every_documented_rejection_without_gpu():
     NULL, ERR, F32, BF16 = B.BL_ERR_NULL, B.BL_ERR_SHAPE, B.BL_F32, B.BL_BF16
     AL, DT, UN = B.BL_ERR_ALIGN, B.BL_ERR_DTYPE, B.BL_ERR_UNSUPPORTED
     cases = [
-        # bl_device_error, bl_probe_mma_s8
+        # bl_device_error
         (L.bl_device_error, (None, 0), NULL),
-        (L.bl_probe_mma_s8, (None, 1024, 8, a, None), NULL),
-        (L.bl_probe_mma_s8, (a, 1024, 8, None, None), NULL),
-        (L.bl_probe_mma_s8, (a, 255, 8, a, None), ERR),
-        (L.bl_probe_mma_s8, (a, 1024, 0, a, None), ERR),
-        (L.bl_probe_mma_s8, (o2, 1024, 8, a, None), AL),
         # packing
         (L.bl_pack_i2s, (None, 1.0, 4, 128, a, None), NULL),
         (L.bl_pack_i2s, (a, 1.0, 0, 128, a, None), ERR),
