@@ -99,6 +99,13 @@ cudaError_t launch_gemv_i2s(const uint8_t* packed, const void* x, bl_dtype xt, v
                             float eps = 0.f);
 cudaError_t launch_gemv_i2s_gate_up(const uint8_t* packed_gate, const uint8_t* packed_up, const void* x, bl_dtype xt,
                                     void* h, bl_dtype ht, int64_t N, int64_t K, cudaStream_t s);
+// The activation-stationary i2_s GEMV (csrc/gemv_i2s_slot.cu): returns
+// cudaErrorNotSupported, having launched nothing, for shapes it has no plan
+// for; launch_gemv_i2s / launch_gemv_i2s_gate_up then use the tiled kernel.
+cudaError_t launch_gemv_i2s_slot(const uint8_t* packed, const void* x, bl_dtype xt, void* y, bl_dtype yt, int64_t N,
+                                 int64_t K, cudaStream_t s, const void* residual, const void* rms_w, float eps);
+cudaError_t launch_gemv_i2s_gate_up_slot(const uint8_t* packed_gate, const uint8_t* packed_up, const void* x,
+                                         bl_dtype xt, void* h, bl_dtype ht, int64_t N, int64_t K, cudaStream_t s);
 cudaError_t launch_gemv_tq2_0(const uint8_t* packed, const void* x, bl_dtype xt, float* y, int64_t N, int64_t K,
                               cudaStream_t s);
 cudaError_t launch_gemm_w1a8(const int8_t* q, const float* sc, const int32_t* wq, const uint16_t* ws,
@@ -122,8 +129,6 @@ cudaError_t launch_gemm_w1a8_act_tiled(const void* x, bl_dtype xt, const int32_t
                                        cudaStream_t st);
 cudaError_t launch_gemm_tq2_0_int8(const int8_t* q, const float* s, const uint8_t* packed, int64_t M, int64_t N,
                                    int64_t K, float* y, cudaStream_t st);
-// Warp-level int8 MMA throughput probe: enqueues the kernel on `s` and sets
-// *ops to the integer operations it performs (out: out_len ints of scratch).
 cudaError_t launch_gemm_i2s_int8_simt(const int8_t* q, const float* sc, const uint8_t* packed, int64_t M, int64_t N,
                                       int64_t K, float* y, int32_t* acc, cudaStream_t s);
 cudaError_t launch_gemm_i2s_int8(const int8_t* q, const float* sc, const uint8_t* packed, int64_t M, int64_t N,

@@ -733,6 +733,8 @@ cudaError_t run(const uint8_t* packed, const uint8_t* packed2, const void* x, vo
 
 cudaError_t launch_gemv_i2s(const uint8_t* packed, const void* x, bl_dtype xt, void* y, bl_dtype yt, int64_t N,
                             int64_t K, cudaStream_t s, const void* residual, const void* rms_w, float eps) {
+  const cudaError_t e = launch_gemv_i2s_slot(packed, x, xt, y, yt, N, K, s, residual, rms_w, eps);
+  if (e != cudaErrorNotSupported) return e;
   const bool xb = xt == BL_BF16, yb = yt == BL_BF16;
   if (xb)
     return yb ? run<2, true, true, 1>(packed, packed, x, y, N, K, s, residual, rms_w, eps)
@@ -743,6 +745,8 @@ cudaError_t launch_gemv_i2s(const uint8_t* packed, const void* x, bl_dtype xt, v
 
 cudaError_t launch_gemv_i2s_gate_up(const uint8_t* packed_gate, const uint8_t* packed_up, const void* x, bl_dtype xt,
                                     void* h, bl_dtype ht, int64_t N, int64_t K, cudaStream_t s) {
+  const cudaError_t e = launch_gemv_i2s_gate_up_slot(packed_gate, packed_up, x, xt, h, ht, N, K, s);
+  if (e != cudaErrorNotSupported) return e;
   const bool xb = xt == BL_BF16, hb = ht == BL_BF16;
   if (xb)
     return hb ? run<2, true, true, 2>(packed_gate, packed_up, x, h, N, K, s)
