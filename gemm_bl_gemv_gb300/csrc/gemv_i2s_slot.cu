@@ -67,6 +67,9 @@ struct SGeom {
   int N, K, nC, NS;   // rows, columns, 128-element groups, slots per row
   int grid, q, rem;   // CTA c takes q rows, plus one when c < rem
   int nl;             // threads per slot
+  int RS;             // bytes per row in shared memory (K / 4)
+  int PS;             // partials per row in shared memory (NS rounded up to odd: conflict-free row reads)
+  int tpr;            // threads adding one row's partials (a power of two <= 32 / NM)
   uint32_t off_rec, off_part, smem;
   unsigned int* err;
   const void* residual;  // NM == 1: added to y (y's dtype), or nullptr
@@ -212,6 +215,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   __shared__ uint64_t wbar;
   __shared__ int abort_flag;
   __shared__ float red[kWarps];
+  __shared__ float tscale[2];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int c = blockIdx.x;
   const int r0 = c * g.q + min(c, g.rem);
@@ -229,9 +233,11 @@ __global__ void __launch_bounds__(kThreads, 2)
     abort_flag = 0;
   }
   __syncthreads();
+  if (tid < NM)  // the tensor scales (after the codes): fetched now, not on the epilogue's critical path
+    tscale[tid] = *reinterpret_cast<const float*>(pk(tid) + int64_t(g.N) * row_bytes);
   for (int t = tid; t < R; t += kThreads) {
     const int m = t / rows, i = t - m * rows;
-    bulk_g2s(smem + size_t(t) * row_bytes, pk(m) + int64_t(r0 + i) * row_bytes, uint32_t(row_bytes), &wbar,
+    bulk_g2s(smem + size_t(t) * g.RS, pk(m) + int64_t(r0 + i) * row_bytes, uint32_t(row_bytes), &wbar,
              policy_evict_first());
   }
   // the next kernel's CTAs may become resident now: they fetch their own
@@ -259,31 +265,43 @@ __global__ void __launch_bounds__(kThreads, 2)
     for (int w = 0; w < kWarps; ++w) tot = __fadd_rn(tot, red[w]);
     rinv = __fdiv_rn(1.f, __fsqrt_rn(__fadd_rn(__fdiv_rn(tot, float(g.K)), g.eps)));
   }
+  // two groups per warp and pass; the next pass's elements are loaded before
+  // this pass is converted, so only the first load's latency is exposed
   const int L = lane & 15;
+  float v[8], wv[8];
+  auto fetch = [&](int gb, float (&a)[8], float (&b)[8]) {
+    const int grp = gb + (lane >> 4);
+    if (gb < g.nC && grp < g.nC) {
+      load8<XB>(x, grp * 128 + 8 * L, a);
+      if (rmsw) load8<XB>(rmsw, grp * 128 + 8 * L, b);
+    }
+  };
+  fetch(2 * warp, v, wv);
   for (int gb = 2 * warp; gb < g.nC; gb += 2 * kWarps) {
+    float vn[8], wn[8];
+    fetch(gb + 2 * kWarps, vn, wn);
     const int grp = gb + (lane >> 4);
     const bool active = grp < g.nC;
-    float v[8];
-    if (active) {
-      load8<XB>(x, grp * 128 + 8 * L, v);
-      if (rmsw) {
-        float wv[8];
-        load8<XB>(rmsw, grp * 128 + 8 * L, wv);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) v[i] = __fmul_rn(__fmul_rn(v[i], rinv), wv[i]);
-      }
-    } else {
-#pragma unroll
-      for (int i = 0; i < 8; ++i) v[i] = 0.f;
+    for (int i = 0; i < 8; ++i) {
+      if (!active) v[i] = 0.f;
+      else if (rmsw) v[i] = __fmul_rn(__fmul_rn(v[i], rinv), wv[i]);
     }
     group_records<D>(v, active, grp, rec, lane);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      v[i] = vn[i];
+      wv[i] = wn[i];
+    }
   }
-  const float sc0 = *reinterpret_cast<const float*>(pk(0) + int64_t(g.N) * row_bytes);
-  const float sc1 = NM == 2 ? *reinterpret_cast<const float*>(pk(1) + int64_t(g.N) * row_bytes) : sc0;
   __syncthreads();
+  const float sc0 = tscale[0], sc1 = tscale[NM - 1];
 
   // ---- slot dot products -------------------------------------------------------
   bool waited = false;
+  // consecutive threads take consecutive slots of the same rows (one 16-byte
+  // row load per thread, a warp's loads contiguous); the nl threads of a slot
+  // take rows j, j + nl, ...
   for (int vs = tid; vs < g.NS * g.nl; vs += kThreads) {
     const int s = vs % g.NS, j = vs / g.NS;
     uint32_t xd[C::kDig];
@@ -308,29 +326,42 @@ __global__ void __launch_bounds__(kThreads, 2)
     for (int row = j; row < R; row += g.nl) {
       uint32_t wd[C::W];
       if constexpr (C::W == 4) {
-        const uint4 q = *reinterpret_cast<const uint4*>(wp + size_t(row) * row_bytes);
+        const uint4 q = *reinterpret_cast<const uint4*>(wp + size_t(row) * g.RS);
         wd[0] = q.x; wd[1] = q.y; wd[2] = q.z; wd[3] = q.w;
       } else {
-        const uint2 q = *reinterpret_cast<const uint2*>(wp + size_t(row) * row_bytes);
+        const uint2 q = *reinterpret_cast<const uint2*>(wp + size_t(row) * g.RS);
         wd[0] = q.x; wd[1] = q.y;
       }
-      part[size_t(row) * g.NS + s] = slot_dot<D>(wd, xd, S, fa, fb);
+      part[size_t(row) * g.PS + s] = slot_dot<D>(wd, xd, S, fa, fb);
     }
   }
   __syncthreads();
 
-  // ---- one warp per output: the row's partials in slot order -------------------
+  // ---- the partials of each row in slot order: tpr threads per row (slots
+  //      tpr apart, in order), then a fixed butterfly; lane 0 of the row keeps
+  //      the result, so it does not depend on timing ------------------------------
   if (!abort_flag) {
-    for (int i = warp; i < rows; i += kWarps) {
-      float a = 0.f, b = 0.f;
-      for (int s = lane; s < g.NS; s += 32) {
-        a += part[size_t(i) * g.NS + s];
-        if (NM == 2) b += part[size_t(rows + i) * g.NS + s];
+    const int per_out = NM * g.tpr;         // threads per output
+    const int opw = 32 / per_out;           // outputs per warp and pass
+    const int sub = lane % per_out, m = sub / g.tpr, l = sub % g.tpr;
+    for (int ob = warp * opw; ob < rows; ob += kWarps * opw) {
+      const int o = ob + lane / per_out;
+      float a = 0.f;
+      if (o < rows) {
+        // up to 16 partials in flight, added in slot order
+        const float* pr = part + size_t(m * rows + o) * g.PS;
+        for (int s0 = l; s0 < g.NS; s0 += 16 * g.tpr) {
+          float t[16];
+#pragma unroll
+          for (int k = 0; k < 16; ++k) t[k] = s0 + k * g.tpr < g.NS ? pr[s0 + k * g.tpr] : 0.f;
+#pragma unroll
+          for (int k = 0; k < 16; ++k) a += t[k];
+        }
       }
-      a = warp_sum(a);
-      if (NM == 2) b = warp_sum(b);
-      if (lane == 0) {
-        const int row = r0 + i;
+      for (int off = g.tpr >> 1; off > 0; off >>= 1) a += __shfl_xor_sync(0xffffffffu, a, off);
+      const float b = NM == 2 ? __shfl_down_sync(0xffffffffu, a, g.tpr) : 0.f;  // the up row's sum
+      if (o < rows && sub == 0) {
+        const int row = r0 + o;
         if (NM == 2) {
           const float gv = fmaxf(a * sc0, 0.f), uv = b * sc1;
           store_out<YB>(y, row, (gv * gv) * uv);
@@ -360,10 +391,16 @@ bool plan_slot(SGeom& g, int64_t N, int64_t K, int max_smem, int nsm) {
   g.q = g.N / g.grid;
   g.rem = g.N % g.grid;
   g.nl = std::max(1, kThreads / g.NS);
-  const uint64_t R = uint64_t(NM) * (g.q + (g.rem ? 1 : 0));
-  const uint64_t off_rec = up(R * uint64_t(K / 4), 128);
+  g.PS = g.NS | 1;
+  g.RS = int(K / 4);
+  const int rows_max = g.q + (g.rem ? 1 : 0);
+  // threads per row for the final sums: as many as fit one pass over the rows, at most NS
+  g.tpr = 32 / NM;
+  while (g.tpr > 1 && ((kThreads / (NM * g.tpr)) < rows_max || g.tpr > g.NS)) g.tpr >>= 1;
+  const uint64_t R = uint64_t(NM) * rows_max;
+  const uint64_t off_rec = up(R * uint64_t(g.RS), 128);
   const uint64_t off_part = up(off_rec + 4ull * g.NS * C::kStride, 128);
-  const uint64_t total = off_part + 4ull * R * g.NS;
+  const uint64_t total = off_part + 4ull * R * g.PS;
   if (total > uint64_t(max_smem)) return false;
   g.off_rec = uint32_t(off_rec);
   g.off_part = uint32_t(off_part);
