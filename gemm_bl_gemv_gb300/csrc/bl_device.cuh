@@ -91,6 +91,26 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;"); }
 
+// ---- thread-block clusters ---------------------------------------------------
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// Every thread of every CTA of the cluster; orders shared-memory writes before it
+// against the other CTAs' reads after it.
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// *p in the shared memory of cluster CTA `rank` (p: this CTA's copy of the variable)
+__device__ __forceinline__ float ld_peer_f32(const float* p, uint32_t rank) {
+  uint32_t a;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(smem_addr(p)), "r"(rank));
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(a) : "memory");
+  return v;
+}
+
 // ---- integer dot products -------------------------------------------------
 // sum over 4 bytes of (unsigned a_i) * (signed b_i) + c
 __device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {

@@ -64,13 +64,15 @@ struct Slot {
 };
 
 struct SGeom {
-  int N, K, nC, NS;   // rows, columns, 128-element groups, slots per row
-  int grid, q, rem;   // CTA c takes q rows, plus one when c < rem
+  int N, K;           // rows, columns
+  int ks;             // CTAs sharing a row range (a cluster), each taking 1/ks of K
+  int nC, NS;         // 128-element groups and slots of a row in one CTA's share of K
+  int grid, q, rem;   // cluster c takes q rows, plus one when c < rem
   int nl;             // threads per slot
-  int RS;             // bytes per row in shared memory (K / 4)
+  int RS;             // bytes per row in shared memory (this CTA's share: 32 nC)
   int PS;             // partials per row in shared memory (NS rounded up to odd: conflict-free row reads)
   int tpr;            // threads adding one row's partials (a power of two <= 32 / NM)
-  uint32_t off_rec, off_part, smem;
+  uint32_t off_rec, off_part, off_sum, smem;
   unsigned int* err;
   const void* residual;  // NM == 1: added to y (y's dtype), or nullptr
   const void* rms_w;     // NM == 1: RMSNorm weights (x's dtype), or nullptr
@@ -217,11 +219,13 @@ __global__ void __launch_bounds__(kThreads, 2)
   __shared__ float red[kWarps];
   __shared__ float tscale[2];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int c = blockIdx.x;
+  const int rank = g.ks == 2 ? int(cluster_ctarank()) : 0;
+  const int c = blockIdx.x / g.ks;
   const int r0 = c * g.q + min(c, g.rem);
   const int rows = g.q + (c < g.rem ? 1 : 0);
   const int R = NM * rows;  // rows in shared memory: matrix m's row i at m * rows + i
   const int64_t row_bytes = g.K / 4;
+  const int gx0 = rank * g.nC;  // first group of this CTA's share of K
   uint32_t* rec = reinterpret_cast<uint32_t*>(smem + g.off_rec);
   float* part = reinterpret_cast<float*>(smem + g.off_part);
   auto pk = [&](int m) { return (NM == 2 && m) ? packed2 : packed; };
@@ -229,7 +233,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   if (tid == 0) {
     mbar_init(&wbar, 1);
     fence_barrier_init();
-    mbar_arrive_expect_tx(&wbar, uint32_t(R) * uint32_t(row_bytes));
+    mbar_arrive_expect_tx(&wbar, uint32_t(R) * uint32_t(g.RS));
     abort_flag = 0;
   }
   __syncthreads();
@@ -237,7 +241,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     tscale[tid] = *reinterpret_cast<const float*>(pk(tid) + int64_t(g.N) * row_bytes);
   for (int t = tid; t < R; t += kThreads) {
     const int m = t / rows, i = t - m * rows;
-    bulk_g2s(smem + size_t(t) * g.RS, pk(m) + int64_t(r0 + i) * row_bytes, uint32_t(row_bytes), &wbar,
+    bulk_g2s(smem + size_t(t) * g.RS, pk(m) + int64_t(r0 + i) * row_bytes + 32 * gx0, uint32_t(g.RS), &wbar,
              policy_evict_first());
   }
   // the next kernel's CTAs may become resident now: they fetch their own
@@ -272,8 +276,8 @@ __global__ void __launch_bounds__(kThreads, 2)
   auto fetch = [&](int gb, float (&a)[8], float (&b)[8]) {
     const int grp = gb + (lane >> 4);
     if (gb < g.nC && grp < g.nC) {
-      load8<XB>(x, grp * 128 + 8 * L, a);
-      if (rmsw) load8<XB>(rmsw, grp * 128 + 8 * L, b);
+      load8<XB>(x, (gx0 + grp) * 128 + 8 * L, a);
+      if (rmsw) load8<XB>(rmsw, (gx0 + grp) * 128 + 8 * L, b);
     }
   };
   fetch(2 * warp, v, wv);
@@ -360,7 +364,9 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
       for (int off = g.tpr >> 1; off > 0; off >>= 1) a += __shfl_xor_sync(0xffffffffu, a, off);
       const float b = NM == 2 ? __shfl_down_sync(0xffffffffu, a, g.tpr) : 0.f;  // the up row's sum
-      if (o < rows && sub == 0) {
+      if (g.ks == 2) {
+        if (o < rows && sub == 0) reinterpret_cast<float*>(smem + g.off_sum)[o] = a;  // this CTA's share
+      } else if (o < rows && sub == 0) {
         const int row = r0 + o;
         if (NM == 2) {
           const float gv = fmaxf(a * sc0, 0.f), uv = b * sc1;
@@ -377,22 +383,47 @@ __global__ void __launch_bounds__(kThreads, 2)
   } else if (tid == 0) {
     mbar_wait_bounded(&wbar, 0, nullptr);  // let the copies still in flight land before the CTA exits
   }
+  if (g.ks == 2) {
+    // the two CTAs' shares of each row, added in rank order; rank r finishes
+    // half of the rows.  Every thread of both CTAs reaches both cluster
+    // barriers, whatever happened before (the second keeps this CTA's shares
+    // readable until the peer is done).
+    cluster_sync();
+    if (NM == 1 && !abort_flag) {
+      const float* sum = reinterpret_cast<const float*>(smem + g.off_sum);
+      const int half = (rows + 1) / 2;
+      for (int o = rank * half + tid; o < min(rows, (rank + 1) * half); o += kThreads) {
+        const float mine = sum[o], peer = ld_peer_f32(sum + o, uint32_t(rank ^ 1));
+        const float a = rank == 0 ? mine + peer : peer + mine;
+        const int row = r0 + o;
+        float out = a * sc0;
+        if (g.residual)
+          out += YB ? bf16_bits_to_f32(reinterpret_cast<const uint16_t*>(g.residual)[row])
+                    : reinterpret_cast<const float*>(g.residual)[row];
+        store_out<YB>(y, row, out);
+      }
+    }
+    cluster_sync();
+  }
 }
 
 template <int D, int NM>
-bool plan_slot(SGeom& g, int64_t N, int64_t K, int max_smem, int nsm) {
+bool plan_slot(SGeom& g, int64_t N, int64_t K, int max_smem, int nsm, int ks) {
   using C = Slot<D>;
   auto up = [](uint64_t v, uint64_t a) { return (v + a - 1) / a * a; };
+  if ((K / 128) % ks || (ks > 1 && NM != 1)) return false;
   g.N = int(N);
   g.K = int(K);
-  g.nC = int(K / 128);
+  g.ks = ks;
+  g.nC = int(K / 128) / ks;
   g.NS = g.nC * C::kPerGroup;
-  g.grid = int(std::min<int64_t>(nsm, N));
-  g.q = g.N / g.grid;
-  g.rem = g.N % g.grid;
+  const int clusters = int(std::min<int64_t>(nsm / ks, N));
+  g.grid = clusters * ks;
+  g.q = g.N / clusters;
+  g.rem = g.N % clusters;
   g.nl = std::max(1, kThreads / g.NS);
   g.PS = g.NS | 1;
-  g.RS = int(K / 4);
+  g.RS = 32 * g.nC;
   const int rows_max = g.q + (g.rem ? 1 : 0);
   // threads per row for the final sums: as many as fit one pass over the rows, at most NS
   g.tpr = 32 / NM;
@@ -400,10 +431,12 @@ bool plan_slot(SGeom& g, int64_t N, int64_t K, int max_smem, int nsm) {
   const uint64_t R = uint64_t(NM) * rows_max;
   const uint64_t off_rec = up(R * uint64_t(g.RS), 128);
   const uint64_t off_part = up(off_rec + 4ull * g.NS * C::kStride, 128);
-  const uint64_t total = off_part + 4ull * R * g.PS;
+  const uint64_t off_sum = up(off_part + 4ull * R * g.PS, 16);
+  const uint64_t total = off_sum + (ks > 1 ? 4ull * rows_max : 0);
   if (total > uint64_t(max_smem)) return false;
   g.off_rec = uint32_t(off_rec);
   g.off_part = uint32_t(off_part);
+  g.off_sum = uint32_t(off_sum);
   g.smem = uint32_t(total);
   return true;
 }
@@ -425,9 +458,13 @@ cudaError_t run_slot(const uint8_t* packed, const uint8_t* packed2, const void* 
     int max_optin = 0;
     cudaDeviceGetAttribute(&max_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
     const int cap = max_optin - 1024;  // static shared memory of the kernel stays below 1 KB
-    // prefer a plan that leaves room for the next launch's CTA on the SM
-    p.ok = plan_slot<D, NM>(p.g, N, K, std::min(cap, kCoResident), sm_count()) ||
-           plan_slot<D, NM>(p.g, N, K, cap, sm_count());
+    // a long K is split over a cluster of two CTAs (each builds half of the
+    // records and takes half of every row); prefer plans that leave room for
+    // the next launch's CTA on the SM
+    const int nsm = sm_count(), co = std::min(cap, kCoResident);
+    const bool split = NM == 1 && K / 128 >= 40;
+    p.ok = (split && plan_slot<D, NM>(p.g, N, K, co, nsm, 2)) || plan_slot<D, NM>(p.g, N, K, co, nsm, 1) ||
+           (split && plan_slot<D, NM>(p.g, N, K, cap, nsm, 2)) || plan_slot<D, NM>(p.g, N, K, cap, nsm, 1);
     if (p.ok) {
       cudaError_t e = raise_smem_cap(kern, dev, cap);
       if (e != cudaSuccess) return e;
@@ -440,7 +477,26 @@ cudaError_t run_slot(const uint8_t* packed, const uint8_t* packed2, const void* 
   p.g.residual = residual;
   p.g.rms_w = rms_w;
   p.g.eps = eps;
-  return launch(kern, dim3(p.g.grid), dim3(kThreads), p.g.smem, st, overlap_enabled(), packed, packed2, x, y, p.g);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.g.grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = p.g.smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  int na = 0;
+  if (overlap_enabled()) {
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na++].val.programmaticStreamSerializationAllowed = 1;
+  }
+  if (p.g.ks > 1) {
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = unsigned(p.g.ks);
+    attr[na].val.clusterDim.y = 1;
+    attr[na++].val.clusterDim.z = 1;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = na;
+  return cudaLaunchKernelEx(&cfg, kern, packed, packed2, x, y, p.g);
 }
 
 }  // namespace
