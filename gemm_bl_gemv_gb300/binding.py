@@ -20,7 +20,7 @@ BL_DEVERR_WAIT_TIMEOUT = 0x1
 BL_DEVERR_RANGE = 0x2
 
 EXPORTS = [
-    "bl_status_string", "bl_last_error", "bl_device_error", "bl_set_overlap", "bl_get_overlap",
+    "bl_status_string", "bl_last_error", "bl_device_error", "bl_set_overlap", "bl_get_overlap", "bl_set_wait_limit",
     "bl_pack_i2s", "bl_pack_tq2_0", "bl_pack_w1", "bl_quantize_act_absmax_int8",
     "bl_gemv_i2s", "bl_gemv_i2s_residual", "bl_gemv_i2s_rmsnorm", "bl_gemv_i2s_gate_up", "bl_gemv_tq2_0", "bl_gemm_w1a8", "bl_gemm_w1a8_act", "bl_gemm_i2s_int8",
     "bl_gemm_tq2_0_int8",
@@ -41,6 +41,7 @@ def _declare(L):
         "bl_device_error": ([p, i32], st),
         "bl_set_overlap": ([i32], None),
         "bl_get_overlap": ([], i32),
+        "bl_set_wait_limit": ([ctypes.c_uint64], st),
         "bl_pack_i2s": ([p, ctypes.c_float, i64, i64, p, p], st),
         "bl_pack_tq2_0": ([p, p, i64, i64, p, p], st),
         "bl_pack_w1": ([p, i64, i64, p, p], st),
@@ -133,6 +134,11 @@ def set_overlap(enable: bool):
 
 def get_overlap() -> bool:
     return bool(_lib.bl_get_overlap())
+
+
+def set_wait_limit(ns: int):
+    """Pipeline waits of later launches give up after ns nanoseconds (0: the default second); test aid."""
+    _check(_lib.bl_set_wait_limit(int(ns)))
 
 
 def device_error(clear: bool = True) -> int:

@@ -15,6 +15,9 @@ namespace bl {
 // The library's device error word (BL_DEVERR_* bits).
 __device__ unsigned int g_dev_error = 0;
 
+std::atomic<unsigned long long> g_wait_limit{0};
+unsigned long long wait_limit_ns() { return g_wait_limit.load(); }
+
 namespace {
 std::atomic<int> g_overlap{0};
 thread_local char g_msg[512] = "";
@@ -150,6 +153,11 @@ bl_status bl_device_error(uint32_t* flags, int clear) {
     e = cudaMemcpyToSymbol(bl::g_dev_error, &z, sizeof(z));
     if (e != cudaSuccess) return cuda_status(e, "bl_device_error clear");
   }
+  return BL_OK;
+}
+
+bl_status bl_set_wait_limit(uint64_t ns) {
+  bl::g_wait_limit.store(ns);
   return BL_OK;
 }
 

@@ -56,19 +56,51 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 
 // Wait for phase `parity` of `bar` to complete, at most kWaitLimitNs.
 // Returns false (and ORs BL_DEVERR_WAIT_TIMEOUT into *err, the library's
-// device error word) on timeout.
+// device error word) on timeout.  Waits that let a CTA's own copies land
+// before it exits pass err = nullptr.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, unsigned int* err) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = globaltimer_ns();
+  const unsigned long long limit = kWaitLimitNs;
   while (true) {
 #pragma unroll 1  // try_wait suspends in hardware for a while: a rolled loop keeps the code small
     for (int i = 0; i < 64; ++i)
       if (mbar_try_wait(bar, parity)) return true;
-    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+    if (globaltimer_ns() - t0 > limit) {
       if (err) atomicOr(err, BL_DEVERR_WAIT_TIMEOUT);
       return false;
     }
   }
+}
+
+// Non-blocking check of phase `parity` of `bar`.
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// A pipeline wait with a launch-given limit: limit_ns = 0 is mbar_wait_bounded;
+// otherwise (a test limit, see bl_set_wait_limit) the barrier is polled
+// without try_wait's hardware suspension, so that a phase still in progress
+// runs the limit out.
+__device__ __forceinline__ bool mbar_wait_limited(uint64_t* bar, uint32_t parity, unsigned int* err,
+                                                  unsigned long long limit_ns) {
+  if (limit_ns == 0) return mbar_wait_bounded(bar, parity, err);
+  const unsigned long long t0 = globaltimer_ns();
+  while (!mbar_test_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > limit_ns) {
+      if (err) atomicOr(err, BL_DEVERR_WAIT_TIMEOUT);
+      return false;
+    }
+  }
+  return true;
 }
 
 // ---- bulk async copy global -> shared (completes on an mbarrier) ----------

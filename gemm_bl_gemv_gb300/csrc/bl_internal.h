@@ -14,6 +14,10 @@ namespace bl {
 // Overlap (programmatic dependent launch) setting, see bl_set_overlap().
 bool overlap_enabled();
 
+// Test limit of the pipeline waits in ns (bl_set_wait_limit), 0 for the
+// default; read at launch time by the kernels that honour it.
+unsigned long long wait_limit_ns();
+
 // Number of SMs of the current device (cached per device).
 int sm_count();
 

@@ -230,11 +230,17 @@ __global__ void __launch_bounds__((MT == 1 ? 512 : 256), (MT >= 2 && MT <= 4 ? 2
       for (int w = 0; w < 8; ++w) {
         if (w >= g.wpc) break;
         const uint32_t* qw = rc + w * 8 * MT;
+        uint32_t q8[8];
+        if (MT == 1) {  // one token: the word's eight class words by two 16-byte loads (records are 16-byte aligned)
+          const uint4 a0 = *reinterpret_cast<const uint4*>(qw), a1 = *reinterpret_cast<const uint4*>(qw + 4);
+          q8[0] = a0.x; q8[1] = a0.y; q8[2] = a0.z; q8[3] = a0.w;
+          q8[4] = a1.x; q8[5] = a1.y; q8[6] = a1.z; q8[7] = a1.w;
+        }
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
           uint32_t qj[MT];  // activation words of class j, one per token (broadcast reads)
 #pragma unroll
-          for (int m = 0; m < MT; ++m) qj[m] = qw[j * MT + m];
+          for (int m = 0; m < MT; ++m) qj[m] = MT == 1 ? q8[j] : qw[j * MT + m];
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
             if (MT == 1) {

@@ -74,6 +74,7 @@ struct SGeom {
   int tpr;            // threads adding one row's partials (a power of two <= 32 / NM)
   uint32_t off_rec, off_part, off_sum, smem;
   unsigned int* err;
+  unsigned long long wait_ns;  // pipeline wait limit (0: the default; a test limit otherwise)
   const void* residual;  // NM == 1: added to y (y's dtype), or nullptr
   const void* rms_w;     // NM == 1: RMSNorm weights (x's dtype), or nullptr
   float eps;
@@ -322,7 +323,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     const float fb = reinterpret_cast<const float*>(r + C::kDig)[D + 1];
     if (!waited) {
       waited = true;
-      if (!abort_flag && !mbar_wait_bounded(&wbar, 0, g.err)) abort_flag = 1;
+      if (!abort_flag && !mbar_wait_limited(&wbar, 0, g.err, g.wait_ns)) abort_flag = 1;
     }
     if (abort_flag) break;
     const uint8_t* wp = smem + size_t(s) * (4 * C::W);
@@ -474,6 +475,7 @@ cudaError_t run_slot(const uint8_t* packed, const uint8_t* packed2, const void* 
   }
   if (!p.ok || (reinterpret_cast<uintptr_t>(x) & 15) || (reinterpret_cast<uintptr_t>(rms_w) & 15))
     return cudaErrorNotSupported;
+  p.g.wait_ns = wait_limit_ns();
   p.g.residual = residual;
   p.g.rms_w = rms_w;
   p.g.eps = eps;

@@ -129,7 +129,7 @@ __global__ void __launch_bounds__(Pol::kMaxThreads) tiled_kernel(typename Pol::A
       // (bounded), then leave.  The error flag is already set.
       if (tid == 0)
         for (int j = i; j < my_tiles && j < i + g.stages; ++j)
-          mbar_wait_bounded(&full[j % g.stages], uint32_t(j / g.stages) & 1u, g.err);
+          mbar_wait_bounded(&full[j % g.stages], uint32_t(j / g.stages) & 1u, nullptr);
       return;
     }
     if (tid == 0 && i + g.stages < my_tiles) issue(i + g.stages);

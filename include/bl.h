@@ -79,6 +79,22 @@ const char* bl_last_error(void);
 bl_status bl_device_error(uint32_t* flags, int clear);
 
 /*
+ * Test aid for the failure path (no counterpart on the pages): the weight
+ * waits of the i2_s GEMV kernels (bl_gemv_i2s, bl_gemv_i2s_residual,
+ * bl_gemv_i2s_rmsnorm and bl_gemv_i2s_gate_up, in their one-CTA-per-SM
+ * resident plan) launched afterwards give up after `ns` nanoseconds of
+ * %globaltimer instead of the default second (ns = 0 restores the default;
+ * the setting is process-wide and read at each launch).  With a test limit
+ * the wait polls without the hardware's suspension, so a copy still in
+ * flight runs the limit out.  A wait that gives up records
+ * BL_DEVERR_WAIT_TIMEOUT, the kernel skips the rest of its work and its
+ * outputs are unspecified; the waits that let a CTA's own copies land before
+ * it exits keep the full second, so the kernel still returns cleanly.  Other
+ * kernels keep the default limit.  Always returns BL_OK.
+ */
+bl_status bl_set_wait_limit(uint64_t ns);
+
+/*
  * Allow back-to-back launches to overlap (programmatic dependent launch).
  * When enabled, the GEMV/GEMM kernels launched afterwards on any stream may
  * start while the previous kernel on the same stream is still running: they

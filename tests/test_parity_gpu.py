@@ -607,6 +607,54 @@ def test_overlap_mode_same_results(B):
     assert all(torch.equal(ref.view(torch.int16), t.view(torch.int16)) for t in outs)
 
 
+@pytest.mark.parametrize("xd,yd,N,K,fused", [("bf16", "bf16", 152 * 48, 8192, False),   # K split over 2-CTA clusters
+                                             ("f32", "f32", 152 * 40, 8192, False)])
+def test_wait_timeout_path(B, xd, yd, N, K, fused):
+    """The bounded-wait failure path on the GPU: with a 1 ns pipeline wait
+    limit, weight waits that are not satisfied at once give up: the launch
+    completes, BL_DEVERR_WAIT_TIMEOUT is recorded and the device stays
+    usable; with the default limit restored the same call is correct again.
+    (Each CTA's rows here, about 100 KB streamed from HBM after an L2 flush,
+    take longer to arrive than the activation records take to build, so its
+    first weight check fails.)"""
+    g = rng(31337 + K + fused)
+    w = ternary(g, N, K)
+    wu = ternary(g, N, K) if fused else None
+    x = rand_x(g, K, xd)
+    packed = B.bl_pack_i2s(to_gpu(w), np.float32(1.25))
+    pu = B.bl_pack_i2s(to_gpu(wu), np.float32(0.75)) if fused else None
+    xg = x_gpu(x, xd)
+    yt = torch.float32 if yd == "f32" else torch.bfloat16
+    props = torch.cuda.get_device_properties(torch.cuda.current_device())
+    flush = torch.empty(2 * int(getattr(props, "L2_cache_size", 0) or (129 << 20)) // 4, dtype=torch.float32,
+                        device="cuda")
+    flush.zero_()  # the freshly packed weights leave L2
+    del flush
+    torch.cuda.synchronize()
+    B.device_error(clear=True)
+    B.set_wait_limit(1)
+    try:
+        if fused:
+            B.bl_gemv_i2s_gate_up(packed, pu, xg, N, K, h_dtype=yt)
+        else:
+            B.bl_gemv_i2s(packed, xg, N, K, y_dtype=yt)
+        torch.cuda.synchronize()
+    finally:
+        B.set_wait_limit(0)
+    assert B.device_error(clear=True) & B.BL_DEVERR_WAIT_TIMEOUT
+    if fused:
+        h = B.bl_gemv_i2s_gate_up(packed, pu, xg, N, K, h_dtype=yt)
+        hv = h.cpu().numpy().astype(np.float64) if yd == "f32" else x_f64(bits16(h), "bf16")
+        ref, cond = O.gemv_i2s_gate_up(O.pack_i2s(w, np.float32(1.25)), O.pack_i2s(wu, np.float32(0.75)),
+                                       x_f64(x, xd), N, K)
+        assert_close(hv, ref, cond, TOL_F32 if yd == "f32" else TOL_BF16, "after timeout (gate/up)")
+    else:
+        y, ref, cond = run_gemv_i2s(B, w, np.float32(1.25), x, xd, yd)
+        assert_close(y, ref, cond, TOL_F32 if yd == "f32" else TOL_BF16, "after timeout")
+    torch.cuda.synchronize()
+    assert B.device_error(clear=True) == 0
+
+
 def test_error_paths(B):
     x = torch.zeros(100, dtype=torch.float32, device="cuda")
     p = torch.zeros(1000, dtype=torch.uint8, device="cuda")
