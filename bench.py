@@ -263,7 +263,7 @@ def time_graph(torch, dist, body, steps, warmup, graph_steps, stream):
 def kernel_source_hash():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "gemm_bl_gemv_gb300", "csrc")
-    for f in ("gemv_i2s.cu", "bl_device.cuh"):  # the kernel's device code
+    for f in ("gemv_i2s_slot.cu", "bl_device.cuh"):  # the kernel's device code
         h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:16]
 
@@ -414,7 +414,7 @@ def bench_ours(args, dist):
                       "(whole replays)" % (gs, args.steps // gs, warm_steps(args.warmup, gs)),
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
                          "frac": round(achieved / hbm, 4), "traffic": profiled_traffic(),
-                         "kernel": "gemv_i2s_kernel<D=2, bf16 x, bf16 y, gate+up>",
+                         "kernel": "gemv_i2s_slot_kernel<D=2, bf16 x, bf16 y, gate+up>",
                          "algorithmic_bytes_per_launch": gate_up_algorithmic_bytes(),
                          "avg_launch_us": round(avg_launch_s * 1e6, 3), "launches_timed": gu_steps,
                          "peak_source": peak_src + " copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"},
@@ -612,9 +612,19 @@ def bench_secondary(args, B, torch, stream, dist, hbm, bf16_peak):
         y = torch.empty((wl.M, wl.N), dtype=torch.float32, device="cuda")
         t = run(lambda i: B.bl_gemm_i2s_int8(q, s, ws[i % cps], wl.N, y=y))
         tops = 2.0 * wl.M * wl.N * wl.K / (t * 1e-3) / 1e12
+        # from bf16 x: the quantization fused into the product's launch, against act-quant + product
+        xg = torch.from_numpy(xb.view(np.int16)).cuda().view(torch.bfloat16)
+        wsp = B.gemm_i2s_int8_act_workspace(wl.M, wl.K)
+        try:  # a reported extra (a cooperative launch inside a graph): it never stops the headline line
+            t_f = run(lambda i: B.bl_gemm_i2s_int8_act(xg, ws[i % cps], wl.N, workspace=wsp, y=y, fuse=True))
+        except Exception as e:  # noqa: BLE001
+            t_f = float("nan")
+            out["i2s_prefill_512_fused_error"] = repr(e)[:200]
+        t_2 = run(lambda i: B.bl_gemm_i2s_int8_act(xg, ws[i % cps], wl.N, workspace=wsp, y=y))
         out[wl.name] = {"value": round(tops, 2), "unit": "TOPS (int8 ops)", "frac_bf16_dense_peak": round(tops / bf16_peak, 4),
-                        "us_per_launch": t * 1e3}
-        del ws
+                        "us_per_launch": t * 1e3, "us_from_bf16_x_one_launch": t_f * 1e3,
+                        "us_from_bf16_x_two_launches": t_2 * 1e3}
+        del ws, wsp
         if not args.no_cublas:
             out.update(bench_cublas(args, torch, stream, dist, run))
     torch.cuda.synchronize()

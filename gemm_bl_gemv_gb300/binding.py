@@ -23,7 +23,7 @@ EXPORTS = [
     "bl_status_string", "bl_last_error", "bl_device_error", "bl_set_overlap", "bl_get_overlap", "bl_set_wait_limit",
     "bl_pack_i2s", "bl_pack_tq2_0", "bl_pack_w1", "bl_quantize_act_absmax_int8",
     "bl_gemv_i2s", "bl_gemv_i2s_residual", "bl_gemv_i2s_rmsnorm", "bl_gemv_i2s_gate_up", "bl_gemv_tq2_0", "bl_gemm_w1a8", "bl_gemm_w1a8_act", "bl_gemm_i2s_int8",
-    "bl_gemm_tq2_0_int8",
+    "bl_gemm_tq2_0_int8", "bl_gemm_i2s_int8_act", "bl_gemm_i2s_int8_act_workspace",
 ]
 
 
@@ -55,6 +55,8 @@ def _declare(L):
         "bl_gemm_w1a8_act": ([p, i32, p, p, p, i64, i64, i64, i32, p, p], st),
         "bl_gemm_i2s_int8": ([p, p, p, i64, i64, i64, p, p, p], st),
         "bl_gemm_tq2_0_int8": ([p, p, p, i64, i64, i64, p, p], st),
+        "bl_gemm_i2s_int8_act": ([p, i32, p, i64, i64, i64, p, p, ctypes.c_size_t, i32, p], st),
+        "bl_gemm_i2s_int8_act_workspace": ([i64, i64], ctypes.c_size_t),
     }
     for name, (args, res) in sig.items():
         f = getattr(L, name)
@@ -292,6 +294,26 @@ def bl_gemm_w1a8_act(x, wq, ws_fp16_bits, bias_bf16_bits=None, group=128, y=None
         y = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
     _check(_lib.bl_gemm_w1a8_act(_ptr(x), _dtype_code(x), _ptr(wq), _ptr(ws_fp16_bits), _ptr(bias_bf16_bits), M, N, K,
                                  group, _ptr(_cuda(y, "y")), _stream(stream)))
+    return y
+
+
+def gemm_i2s_int8_act_workspace(M, K, device="cuda"):
+    """A zero-filled workspace for bl_gemm_i2s_int8_act (uint8, 256-byte aligned by the allocator)."""
+    n = int(_lib.bl_gemm_i2s_int8_act_workspace(int(M), int(K)))
+    return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
+def bl_gemm_i2s_int8_act(x, packed, N, workspace=None, y=None, fuse=False, stream=None):
+    """bl_quantize_act_absmax_int8(x) then bl_gemm_i2s_int8 in one call (fuse: one launch where it fits)."""
+    for t, n in ((x, "x"), (packed, "packed")):
+        _cuda(t, n)
+    M, K = x.shape
+    if workspace is None:
+        workspace = gemm_i2s_int8_act_workspace(M, K, x.device)
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float32, device=x.device)
+    _check(_lib.bl_gemm_i2s_int8_act(_ptr(x), _dtype_code(x), _ptr(packed), M, N, K, _ptr(_cuda(y, "y")),
+                                     _ptr(workspace), workspace.numel(), 1 if fuse else 0, _stream(stream)))
     return y
 
 

@@ -137,5 +137,11 @@ cudaError_t launch_gemm_i2s_int8_simt(const int8_t* q, const float* sc, const ui
                                       int64_t K, float* y, int32_t* acc, cudaStream_t s);
 cudaError_t launch_gemm_i2s_int8(const int8_t* q, const float* sc, const uint8_t* packed, int64_t M, int64_t N,
                                  int64_t K, float* y, int32_t* acc, cudaStream_t s);
+// The prefill from unquantized activations (act quantization fused in); ws
+// as laid out by gemm_i2s_int8_act_workspace (barrier words zero before the
+// first use).
+size_t gemm_i2s_int8_act_workspace(int64_t M, int64_t K);
+cudaError_t launch_gemm_i2s_int8_act(const void* x, bl_dtype xt, const uint8_t* packed, int64_t M, int64_t N,
+                                     int64_t K, float* y, uint8_t* ws, int fuse, cudaStream_t s);
 
 }  // namespace bl

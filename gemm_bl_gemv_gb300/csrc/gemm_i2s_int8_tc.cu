@@ -32,6 +32,7 @@
 //     copy (acc likewise when asked).
 // Every wait is bounded; on a timeout the CTA records the error flag,
 // finishes its loops without waiting, and still frees its TMEM.
+#include "act_quant.cuh"
 #include "bl_device.cuh"
 #include "bl_internal.h"
 
@@ -105,10 +106,103 @@ __device__ __forceinline__ void i8x4_to_f16_scaled(uint32_t v, uint32_t sc, uint
   hi = hfma2(__byte_perm(x, 0x64u, 0x4342), sc, bias);
 }
 
+// Workspace of the fused form: two barrier words at its start (count,
+// generation), then q [M][K] at byte 256, then s [M] at the next 256 bytes.
+constexpr size_t kWsQ = 256;
+__host__ __device__ constexpr size_t ws_s_offset(size_t M, size_t K) { return kWsQ + (M * K + 255) / 256 * 256; }
+
+// Fused quantization, before the product (cooperative launch: every CTA is
+// resident).  The CTAs split the tokens; the warps 0-15 of a CTA take its
+// tokens 16 / wpt at a time (wpt warps per token, a power of two), each
+// thread taking 8-element chunks: a first sweep finds the token's absmax, a
+// second (the same chunks, from L1) writes the codes.  Then a grid barrier: the last CTA to arrive resets the count and
+// advances the generation the others wait on (bounded), so the workspace's
+// barrier words are back in their initial state after every call.
+template <bool XB>
+__device__ __forceinline__ bool quantize_and_sync(const void* x, int M, int K, int8_t* q, float* sc,
+                                                  unsigned int* bar, unsigned int* err) {
+  __shared__ float red[16];
+  const int G = int(gridDim.x * gridDim.y), cta = int(blockIdx.y * gridDim.x + blockIdx.x);
+  const int t0 = int(int64_t(cta) * M / G), t1 = int(int64_t(cta + 1) * M / G);
+  const int nt = t1 - t0;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  int wpt = 16;
+  while (wpt > 1 && wpt * nt > 16) wpt >>= 1;
+  const int tp = 16 / wpt;  // tokens per pass
+  const int tok = warp / wpt, wi = warp % wpt;
+  const int n8 = K / 8, tt = 32 * wpt, i0 = 32 * wi + lane;
+  const size_t row_bytes = size_t(K) * (XB ? 2 : 4);
+  for (int base = 0; base < nt; base += tp) {
+    const int m = t0 + base + tok;
+    const bool active = warp < 16 && base + tok < nt;
+    const void* xr = reinterpret_cast<const uint8_t*>(x) + size_t(active ? m : 0) * row_bytes;
+    float a = 0.f;
+    if (active)
+      for (int k8 = i0; k8 < n8; k8 += tt) {
+        float v[8];
+        load8<XB>(xr, k8, v);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) a = fmaxf(a, fabsf(v[j]));
+      }
+    a = warp_max(a);
+    if (warp < 16 && lane == 0) red[warp] = a;
+    __syncthreads();
+    if (active) {
+      float amax = 0.f;
+      for (int w = tok * wpt; w < (tok + 1) * wpt; ++w) amax = fmaxf(amax, red[w]);
+      float s_m, inv;
+      absmax_scales(amax, s_m, inv);
+      if (i0 == 0) sc[m] = s_m;
+      uint2* qr = reinterpret_cast<uint2*>(q + size_t(m) * K);
+      for (int k8 = i0; k8 < n8; k8 += tt) {
+        float v[8];
+        load8<XB>(xr, k8, v);
+        qr[k8] = quant8(v, inv);
+      }
+    }
+    __syncthreads();  // red is reused by the next pass
+  }
+  asm volatile("fence.proxy.async.global;" ::: "memory");  // the product reads q through TMA
+  __syncthreads();
+  __shared__ int ok;
+  if (threadIdx.x == 0) {
+    ok = 1;
+    volatile unsigned int* vgen = bar + 1;
+    const unsigned int gen = *vgen;
+    __threadfence();
+    if (atomicAdd(bar, 1u) == unsigned(G - 1)) {
+      bar[0] = 0u;
+      __threadfence();
+      atomicAdd(bar + 1, 1u);
+    } else {
+      const unsigned long long start = globaltimer_ns();
+      while (true) {
+        unsigned int g;
+        asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(g) : "l"(bar + 1) : "memory");
+        if (g != gen) break;
+        if (globaltimer_ns() - start > kWaitLimitNs) {
+          atomicOr(err, BL_DEVERR_WAIT_TIMEOUT);
+          ok = 0;
+          break;
+        }
+        __nanosleep(64);
+      }
+    }
+    __threadfence();
+  }
+  __syncthreads();
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+  return ok != 0;
+}
+
+// XQ = 0: q and s given.  XQ = 1 (fp32 x) / 2 (bf16 x): x given; the codes
+// and scales go to the workspace (ws) first, and qmap describes its q.
+template <int XQ>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_i2s_int8_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap wmap,
                             const float* __restrict__ s, const uint8_t* __restrict__ packed, int M, int N, int K,
-                            float* __restrict__ y, int32_t* __restrict__ acc_out, unsigned int* err) {
+                            float* __restrict__ y, int32_t* __restrict__ acc_out, unsigned int* err,
+                            const void* __restrict__ x, uint8_t* __restrict__ ws) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   uint8_t* araw = smem + kAOff;
@@ -146,6 +240,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   pdl_wait();
+  if (XQ) {
+    int8_t* wq = reinterpret_cast<int8_t*>(ws + kWsQ);
+    float* ws_s = reinterpret_cast<float*>(ws + ws_s_offset(size_t(M), size_t(K)));
+    if (!quantize_and_sync<XQ == 2>(x, M, K, wq, ws_s, reinterpret_cast<unsigned int*>(ws), err) &&
+        threadIdx.x == 0)
+      *abort_flag = 1;
+    s = ws_s;
+    __syncthreads();
+  }
 
   if (warp < kAWarps) {
     // ------- activation converters: TMEM lane / tile row ra = 32 (w % 4) +
@@ -376,11 +479,58 @@ cudaError_t launch_gemm_i2s_int8(const int8_t* q, const float* sc, const uint8_t
   if (!encode_tmap_2d_u8(&qmap, q, uint64_t(K), uint64_t(M), uint64_t(K), BK, BM, true) ||
       !encode_tmap_2d_u8(&wmap, packed, uint64_t(K / 4), uint64_t(N), uint64_t(K / 4), BK / 4, BN, false))
     return cudaErrorNotSupported;
-  cudaError_t e = raise_smem_cap(gemm_i2s_int8_tc_kernel, dev, int(kSmem));
+  cudaError_t e = raise_smem_cap(gemm_i2s_int8_tc_kernel<0>, dev, int(kSmem));
   if (e != cudaSuccess) return e;
   dim3 grid(unsigned((N + BN - 1) / BN), unsigned((M + BM - 1) / BM));
-  return launch(gemm_i2s_int8_tc_kernel, grid, dim3(kThreads), kSmem, s, overlap_enabled(), qmap, wmap, sc, packed,
-                int(M), int(N), int(K), y, acc, dev_error_ptr());
+  return launch(gemm_i2s_int8_tc_kernel<0>, grid, dim3(kThreads), kSmem, s, overlap_enabled(), qmap, wmap, sc, packed,
+                int(M), int(N), int(K), y, acc, dev_error_ptr(), static_cast<const void*>(nullptr),
+                static_cast<uint8_t*>(nullptr));
+}
+
+size_t gemm_i2s_int8_act_workspace(int64_t M, int64_t K) {
+  return ws_s_offset(size_t(M), size_t(K)) + (size_t(M) * 4 + 255) / 256 * 256;
+}
+
+// The product from unquantized x: act-quant into the workspace, then the
+// product (two launches); with `fuse`, one cooperative launch (quantization,
+// grid barrier, product) when every CTA fits on the GPU at once and x's rows
+// are 16-byte aligned with K % 8 == 0.
+cudaError_t launch_gemm_i2s_int8_act(const void* x, bl_dtype xt, const uint8_t* packed, int64_t M, int64_t N,
+                                     int64_t K, float* y, uint8_t* ws, int fuse, cudaStream_t s) {
+  int8_t* q = reinterpret_cast<int8_t*>(ws + kWsQ);
+  float* sc = reinterpret_cast<float*>(ws + ws_s_offset(size_t(M), size_t(K)));
+  const bool xb = xt == BL_BF16;
+  const int64_t tiles = ((N + BN - 1) / BN) * ((M + BM - 1) / BM);
+  const bool one = fuse && M >= 64 && K % 8 == 0 && (reinterpret_cast<uintptr_t>(x) & 15) == 0 &&
+                   (K * (xb ? 2 : 4)) % 16 == 0 && tiles <= sm_count();
+  if (!one) {
+    cudaError_t e = launch_act_quant(x, xt, M, K, q, sc, s);
+    if (e != cudaSuccess) return e;
+    return launch_gemm_i2s_int8(q, sc, packed, M, N, K, y, nullptr, s);
+  }
+  int dev = 0;
+  cudaGetDevice(&dev);
+  CUtensorMap qmap, wmap;
+  if (!encode_tmap_2d_u8(&qmap, q, uint64_t(K), uint64_t(M), uint64_t(K), BK, BM, true) ||
+      !encode_tmap_2d_u8(&wmap, packed, uint64_t(K / 4), uint64_t(N), uint64_t(K / 4), BK / 4, BN, false))
+    return cudaErrorNotSupported;
+  auto kern = xb ? gemm_i2s_int8_tc_kernel<2> : gemm_i2s_int8_tc_kernel<1>;
+  cudaError_t e = raise_smem_cap(kern, dev, int(kSmem));
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned((N + BN - 1) / BN), unsigned((M + BM - 1) / BM));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeCooperative;  // the grid barrier needs every CTA resident
+  attr[0].val.cooperative = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = overlap_enabled() ? 2 : 1;
+  return cudaLaunchKernelEx(&cfg, kern, qmap, wmap, static_cast<const float*>(nullptr), packed, int(M), int(N),
+                            int(K), y, static_cast<int32_t*>(nullptr), dev_error_ptr(), x, ws);
 }
 
 }  // namespace bl

@@ -332,6 +332,34 @@ bl_status bl_gemm_tq2_0_int8(const int8_t* q, const float* s, const uint8_t* pac
 bl_status bl_gemm_i2s_int8(const int8_t* q, const float* s, const uint8_t* packed, int64_t M, int64_t N, int64_t K,
                            float* y, int32_t* acc, bl_stream_t stream);
 
+/*
+ * The i2_s prefill from unquantized activations, in one call
+ * [BG "API" binary_linear = quantize_activation + the product;
+ * BL "BitLinear Mathematics"]: bl_quantize_act_absmax_int8 then
+ * bl_gemm_i2s_int8.
+ *   x : [M, K] fp32 (xt = BL_F32) or bf16 (BL_BF16);  packed, y as for
+ *   bl_gemm_i2s_int8.  The codes, scales and y are bit for bit those of the
+ *   two calls.
+ *   workspace : device memory of at least bl_gemm_i2s_int8_act_workspace(M,
+ *   K) bytes, 256-byte aligned, zero-filled before its first use; owned by
+ *   the caller.  It receives the int8 codes [M, K] at byte 256 and the
+ *   scales (fp32 [M]) at the next 256-byte boundary after them; its first 8
+ *   bytes are grid-barrier words that every call leaves as it found them.
+ *   Calls that share a workspace must not overlap on the GPU.
+ *   fuse : 0 runs the two launches through the workspace (the faster form on
+ *   GB300: 22.1 us for 512 x 2560 bf16 tokens against 6912 rows); 1 fuses the
+ *   quantization into the product's launch when M >= 64, K % 8 == 0, x's
+ *   rows are 16-byte aligned and the product's CTAs (one per 128 x 192 tile)
+ *   fit on the GPU at once: the CTAs quantize their share of the tokens, meet
+ *   at a grid barrier (bounded: a timeout sets BL_DEVERR_WAIT_TIMEOUT) and
+ *   run the product (23.3 us for the same shape); otherwise the two launches.
+ * Requires what bl_gemm_i2s_int8 requires of M, N, K, packed and y; x
+ * aligned to its element size.
+ */
+size_t bl_gemm_i2s_int8_act_workspace(int64_t M, int64_t K);
+bl_status bl_gemm_i2s_int8_act(const void* x, bl_dtype xt, const uint8_t* packed, int64_t M, int64_t N, int64_t K,
+                               float* y, void* workspace, size_t workspace_bytes, int fuse, bl_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -168,7 +168,16 @@ def test_every_documented_rejection_without_gpu():
         (L.bl_gemm_i2s_int8, (a, a, a, 4, 4, 192, a, None, None), ERR),
         (L.bl_gemm_i2s_int8, (a, o4, a, 4, 4, 128, a, None, None), AL),
         (L.bl_gemm_i2s_int8, (a, a, a, 4, 4, 128, a, o4, None), AL),
+        (L.bl_gemm_i2s_int8_act, (a, BF16, a, 4, 4, 128, a, None, 1 << 20, 0, None), NULL),
+        (L.bl_gemm_i2s_int8_act, (a, 7, a, 4, 4, 128, a, a, 1 << 20, 0, None), DT),
+        (L.bl_gemm_i2s_int8_act, (a, BF16, a, 4, 4, 192, a, a, 1 << 20, 0, None), ERR),
+        (L.bl_gemm_i2s_int8_act, (a, BF16, a, 64, 4, 131072 + 128, a, a, 1 << 30, 0, None), UN),
+        (L.bl_gemm_i2s_int8_act, (a, BF16, a, 4, 4, 128, a, a, 256, 0, None), ERR),    # workspace too small
+        (L.bl_gemm_i2s_int8_act, (a, BF16, a, 4, 4, 128, a, P(A + 16), 1 << 20, 0, None), AL),
+        (L.bl_gemm_i2s_int8_act, (P(A + 1), BF16, a, 4, 4, 128, a, a, 1 << 20, 0, None), AL),
     ]
+    assert L.bl_gemm_i2s_int8_act_workspace(512, 2560) == 256 + 512 * 2560 + 2048
+    assert L.bl_gemm_i2s_int8_act_workspace(0, 2560) == 0
     for fn, args, want in cases:
         got = fn(*args)
         assert got == want, (fn.__name__, args, B.status_name(got), B.status_name(want), L.bl_last_error())

@@ -569,6 +569,62 @@ def test_gemm_i2s_int8_workload_prefill(B):
     assert_close(y.cpu().numpy()[:, rows], yref, cond, TOL_F32, "prefill workload")
 
 
+@pytest.mark.parametrize("fuse", [False, True])
+@pytest.mark.parametrize("xd", ["bf16", "f32"])
+@pytest.mark.parametrize("M,N,K", [(64, 200, 1024), (130, 385, 2560), (512, 96, 384), (5, 70, 256), (200, 1, 256)])
+def test_gemm_i2s_int8_act_fused(B, xd, M, N, K, fuse):
+    """The prefill from unquantized x in one call, as two launches or with
+    the quantization fused into the product's launch: the workspace's codes
+    and scales equal bl_quantize_act_absmax_int8's, y equals the two-call
+    bl_gemm_i2s_int8 bit for bit and the oracle within tolerance; a second
+    call on the same workspace (its barrier words reset by the first) gives
+    the same bits.  M < 64 always takes the two launches."""
+    g = rng(17 * M + N + K + (xd == "f32"))
+    w = ternary(g, N, K)
+    x = synth.normal_f32(g, (M, K)) * g.uniform(0.1, 10, (M, 1)).astype(np.float32)
+    x[1, :] = 0.0                      # an all-zero token
+    if xd == "bf16":
+        x = synth.f32_to_bf16_bits(x)
+    xg = x_gpu(x, xd)
+    sw = np.float32(1.5)
+    packed = B.bl_pack_i2s(to_gpu(w), sw)
+    ws = B.gemm_i2s_int8_act_workspace(M, K)
+    y = B.bl_gemm_i2s_int8_act(xg, packed, N, workspace=ws, fuse=fuse)
+    torch.cuda.synchronize()
+    q, s = B.bl_quantize_act_absmax_int8(xg)
+    qo = ws[256:256 + M * K].view(M, K).view(torch.int8)
+    so_off = 256 + (M * K + 255) // 256 * 256
+    so = ws[so_off:so_off + 4 * M].view(torch.float32)
+    assert torch.equal(qo, q) and torch.equal(so.view(torch.int32), s.view(torch.int32))
+    y2 = B.bl_gemm_i2s_int8(q, s, packed, N)
+    assert torch.equal(y.view(torch.int32), y2.view(torch.int32)), "fused must equal the two-call sequence"
+    y3 = B.bl_gemm_i2s_int8_act(xg, packed, N, workspace=ws, fuse=fuse)
+    assert torch.equal(y.view(torch.int32), y3.view(torch.int32))
+    qr, sr = O.quantize_act_absmax_int8(x, xd)
+    aref, yref, cond = O.gemm_i2s_int8(qr, sr, O.pack_i2s(w, sw), N, K)
+    assert_close(y.cpu().numpy(), yref, cond, TOL_F32, "prefill act %dx%dx%d" % (M, N, K))
+
+
+@pytest.mark.parametrize("fuse", [False, True])
+def test_gemm_i2s_int8_act_workload_prefill(B, fuse):
+    """The prefill workload (512 tokens, 2560 -> 6912) from bf16 x in one
+    call: y equals the two-call sequence bit for bit; sampled columns within tolerance."""
+    wl = synth.WORKLOADS["i2s_prefill_512"]
+    M, N, K = wl.M, wl.N, wl.K
+    w = synth.weight_matrix(wl.index, "w", N, K, "ternary", wl.p_zero)
+    sw = synth.tensor_scale(wl.index)
+    xb = synth.activations(wl.index, M, K, "bf16")
+    packed = B.bl_pack_i2s(to_gpu(w), sw)
+    xg = bf16_gpu(xb)
+    y = B.bl_gemm_i2s_int8_act(xg, packed, N, fuse=fuse)
+    q, s = B.bl_quantize_act_absmax_int8(xg)
+    assert torch.equal(y.view(torch.int32), B.bl_gemm_i2s_int8(q, s, packed, N).view(torch.int32))
+    rows = np.unique(np.concatenate([[0, N - 1], rng(19).integers(0, N, 40)]))
+    qr, sr = O.quantize_act_absmax_int8(xb, "bf16")
+    _, yref, cond = O.gemm_i2s_int8(qr, sr, O.pack_i2s(w, sw), N, K, rows=rows)
+    assert_close(y.cpu().numpy()[:, rows], yref, cond, TOL_F32, "prefill act workload")
+
+
 # ---------------------------------------------------------------------------
 # determinism, overlap switch, error paths
 # ---------------------------------------------------------------------------
