@@ -24,6 +24,7 @@ EXPORTS = [
     "bl_pack_i2s", "bl_pack_tq2_0", "bl_pack_w1", "bl_quantize_act_absmax_int8",
     "bl_gemv_i2s", "bl_gemv_i2s_residual", "bl_gemv_i2s_rmsnorm", "bl_gemv_i2s_gate_up", "bl_gemv_tq2_0", "bl_gemm_w1a8", "bl_gemm_w1a8_act", "bl_gemm_i2s_int8",
     "bl_gemm_tq2_0_int8", "bl_gemm_i2s_int8_act", "bl_gemm_i2s_int8_act_workspace",
+    "bl_gemm_i2s_int8_act_noalloc",
 ]
 
 
@@ -57,6 +58,7 @@ def _declare(L):
         "bl_gemm_tq2_0_int8": ([p, p, p, i64, i64, i64, p, p], st),
         "bl_gemm_i2s_int8_act": ([p, i32, p, i64, i64, i64, p, p, ctypes.c_size_t, i32, p], st),
         "bl_gemm_i2s_int8_act_workspace": ([i64, i64], ctypes.c_size_t),
+        "bl_gemm_i2s_int8_act_noalloc": ([p, i32, p, i64, i64, i64, p, i32, p], st),
     }
     for name, (args, res) in sig.items():
         f = getattr(L, name)

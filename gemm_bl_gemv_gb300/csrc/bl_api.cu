@@ -339,6 +339,26 @@ bl_status bl_gemm_i2s_int8(const int8_t* q, const float* s, const uint8_t* packe
   return launch_status(launch_gemm_i2s_int8(q, s, packed, M, N, K, y, acc, S(stream)), "bl_gemm_i2s_int8");
 }
 
+bl_status bl_gemm_i2s_int8_act_noalloc(const void* x, bl_dtype xt, const uint8_t* packed, int64_t M, int64_t N,
+                                       int64_t K, float* y, int fuse, bl_stream_t stream) {
+  if (!x || !packed || !y) return fail(BL_ERR_NULL, "bl_gemm_i2s_int8_act_noalloc: NULL pointer");
+  if (xt != BL_F32 && xt != BL_BF16) return fail(BL_ERR_DTYPE, "bl_gemm_i2s_int8_act_noalloc: bad dtype %d", int(xt));
+  if (M < 1 || N < 1 || K < 128 || K % 128 || N > 0x7fffffff || M > 0x7fffffff)
+    return fail(BL_ERR_SHAPE, "bl_gemm_i2s_int8_act_noalloc: need M, N >= 1, K %% 128 == 0 (M=%lld N=%lld K=%lld)",
+                (long long)M, (long long)N, (long long)K);
+  if (K > 131072)
+    return fail(BL_ERR_UNSUPPORTED, "bl_gemm_i2s_int8_act_noalloc: K <= 131072 supported (K=%lld)", (long long)K);
+  if (M > (int64_t(1) << 40) / K || bl::gemm_i2s_int8_act_workspace(M, K) > bl::gemm_i2s_int8_act_noalloc_limit())
+    return fail(BL_ERR_UNSUPPORTED,
+                "bl_gemm_i2s_int8_act_noalloc: M=%lld, K=%lld needs more workspace than the static %zu bytes; "
+                "use bl_gemm_i2s_int8_act with a workspace", (long long)M, (long long)K,
+                bl::gemm_i2s_int8_act_noalloc_limit());
+  if (!aligned(packed, 16) || !aligned(y, 16) || !aligned(x, xt == BL_F32 ? 4 : 2))
+    return fail(BL_ERR_ALIGN, "bl_gemm_i2s_int8_act_noalloc: packed and y 16-byte, x element aligned");
+  return launch_status(bl::launch_gemm_i2s_int8_act_noalloc(x, xt, packed, M, N, K, y, fuse, S(stream)),
+                       "bl_gemm_i2s_int8_act_noalloc");
+}
+
 size_t bl_gemm_i2s_int8_act_workspace(int64_t M, int64_t K) {
   if (M < 1 || K < 1) return 0;
   return bl::gemm_i2s_int8_act_workspace(M, K);

@@ -143,5 +143,10 @@ cudaError_t launch_gemm_i2s_int8(const int8_t* q, const float* sc, const uint8_t
 size_t gemm_i2s_int8_act_workspace(int64_t M, int64_t K);
 cudaError_t launch_gemm_i2s_int8_act(const void* x, bl_dtype xt, const uint8_t* packed, int64_t M, int64_t N,
                                      int64_t K, float* y, uint8_t* ws, int fuse, cudaStream_t s);
+// The same with the workspace in the library's static device array
+// (csrc/prefill_noalloc.cu), whose size gemm_i2s_int8_act_noalloc_limit gives.
+size_t gemm_i2s_int8_act_noalloc_limit();
+cudaError_t launch_gemm_i2s_int8_act_noalloc(const void* x, bl_dtype xt, const uint8_t* packed, int64_t M, int64_t N,
+                                             int64_t K, float* y, int fuse, cudaStream_t s);
 
 }  // namespace bl

@@ -360,6 +360,32 @@ size_t bl_gemm_i2s_int8_act_workspace(int64_t M, int64_t K);
 bl_status bl_gemm_i2s_int8_act(const void* x, bl_dtype xt, const uint8_t* packed, int64_t M, int64_t N, int64_t K,
                                float* y, void* workspace, size_t workspace_bytes, int fuse, bl_stream_t stream);
 
+/*
+ * bl_gemm_i2s_int8_act without a workspace argument, for callers that
+ * cannot allocate device memory: code handed only its input and output
+ * pointers by a host program that owns all device memory (a plugin, an
+ * inference server's callback), or a loop that must not call cudaMalloc
+ * (it can synchronize the device and fail under memory pressure).  The pages
+ * have no counterpart; this is an interface convenience.
+ * The workspace is a static device array of
+ * BL_GEMM_I2S_INT8_ACT_NOALLOC_WORKSPACE bytes inside the library, which
+ * every GPU that loads the library holds until the process exits; nothing is
+ * allocated at call time.  The first call on a device looks up the array's
+ * device address (cudaGetSymbolAddress, with that device current): make that
+ * first call before any stream capture.  All calls share the one array,
+ * which keeps the last call's contents (the codes and scales of the last
+ * call; each call rewrites them, and the single-launch form clears its
+ * barrier words on the stream first), so calls that overlap on the GPU race
+ * and give wrong results: issue them on one stream, or order them.
+ * Arguments, results and fuse as for bl_gemm_i2s_int8_act.  Returns
+ * BL_ERR_UNSUPPORTED, before any launch, when
+ * bl_gemm_i2s_int8_act_workspace(M, K) exceeds the array (8 MiB: M * K up
+ * to about 8.3 million, e.g. 2048 tokens with K = 3968).
+ */
+#define BL_GEMM_I2S_INT8_ACT_NOALLOC_WORKSPACE (8u << 20)
+bl_status bl_gemm_i2s_int8_act_noalloc(const void* x, bl_dtype xt, const uint8_t* packed, int64_t M, int64_t N,
+                                       int64_t K, float* y, int fuse, bl_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
