@@ -116,6 +116,13 @@ cudaError_t launch_gemm_w1a8(const int8_t* q, const float* sc, const int32_t* wq
                              const uint16_t* bias, int64_t M, int64_t N, int64_t K, int group, uint16_t* y,
                              int32_t* dots, cudaStream_t s);
 bool w1a8_rows_applicable(int64_t M, int64_t K, int G);
+// One token with 128-element groups (csrc/gemm_w1a8_m1.cu); x != nullptr
+// quantizes x (xt) in the kernel instead of taking q and s.  Returns
+// cudaErrorNotSupported, having launched nothing, when it has no plan.
+bool w1a8_m1_applicable(int64_t M, int64_t N, int64_t K, int G);
+cudaError_t launch_gemm_w1a8_m1(const int8_t* q, const float* s, const void* x, bl_dtype xt, const int32_t* wq,
+                                const uint16_t* ws, const uint16_t* bias, int64_t N, int64_t K, uint16_t* y,
+                                int32_t* dots, cudaStream_t st);
 bool w1a8_tc_applicable(int64_t M, int64_t K, int G);
 cudaError_t launch_gemm_w1a8_tc(const int8_t* q, const float* s, const int32_t* wq, const uint16_t* ws,
                                 const uint16_t* bias, int64_t M, int64_t N, int64_t K, int G, uint16_t* y,

@@ -247,6 +247,10 @@ cudaError_t launch_gemm_w1a8(const int8_t* q, const float* s, const int32_t* wq,
     if (dots || !w1a8_tc_applicable(M, K, group)) return cudaErrorNotSupported;
     return launch_gemm_w1a8_tc(q, s, wq, ws, bias, M, N, K, group, y, st);
   }
+  if (w1a8_m1_applicable(M, N, K, group)) {
+    const cudaError_t e = launch_gemm_w1a8_m1(q, s, nullptr, BL_F32, wq, ws, bias, N, K, y, dots, st);
+    if (e != cudaErrorNotSupported) return e;
+  }
   if (w1a8_rows_applicable(M, K, group)) {
     const cudaError_t e = launch_gemm_w1a8_rows(q, s, wq, ws, bias, M, N, K, group, y, dots, st);
     if (e != cudaErrorNotSupported) return e;

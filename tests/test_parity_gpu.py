@@ -418,6 +418,32 @@ def test_gemm_w1a8_small(B, M, G, N, K):
     assert_close(x_f64(yb, "bf16"), yref, cond, TOL_BF16, "w1a8 M=%d G=%d %dx%d" % (M, G, N, K))
 
 
+@pytest.mark.parametrize("N,K", [(14616, 1024), (1000, 5120), (64, 128), (7296, 2560), (8, 65536)])
+def test_gemm_w1a8_one_token(B, N, K):
+    """One token, 128-element groups (the activation-stationary kernel):
+    several tiles per CTA with a ragged last tile, one group per row, the
+    longest K it takes; exact group dots, y with and without the dots
+    output identical, a bias, and the act quantization fused in equal to the
+    two calls."""
+    G = 128
+    g = rng(N + K)
+    w = synth.signs(g, (N, K))
+    xb = rand_x(g, K, "bf16", 1)
+    q, s = O.quantize_act_absmax_int8(xb, "bf16")
+    ws = synth.abs_normal_fp16_bits(g, (N, K // G), 0.02)
+    ws[0, 0] = 0x0001  # fp16 subnormal
+    bias = synth.f32_to_bf16_bits(synth.normal_f32(g, (N,)))
+    wq = B.bl_pack_w1(to_gpu(w))
+    y, dots = B.bl_gemm_w1a8(to_gpu(q), to_gpu(s), wq, fp16_gpu(ws), bf16_gpu(bias), group=G, group_dots=True)
+    y2 = B.bl_gemm_w1a8(to_gpu(q), to_gpu(s), wq, fp16_gpu(ws), bf16_gpu(bias), group=G)
+    assert torch.equal(y.view(torch.int16), y2.view(torch.int16))
+    dref, yref, cond = O.gemm_w1a8(q, s, O.pack_w1(w), ws, bias, K, G)
+    assert np.array_equal(dots.cpu().numpy().astype(np.int64), dref), "group dots must be bit-exact"
+    assert_close(x_f64(bits16(y), "bf16"), yref, cond, TOL_BF16, "w1a8 one token %dx%d" % (N, K))
+    y3 = B.bl_gemm_w1a8_act(bf16_gpu(xb), wq, fp16_gpu(ws), bf16_gpu(bias), group=G)
+    assert torch.equal(y3.view(torch.int16), y2.view(torch.int16)), "fused quantization must equal the two calls"
+
+
 def test_gemm_w1a8_no_dots_matches_dots_variant(B):
     g = rng(77)
     M, N, K, G = 4, 300, 1024, 128
