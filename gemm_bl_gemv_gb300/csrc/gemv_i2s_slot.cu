@@ -355,13 +355,15 @@ __global__ void __launch_bounds__(kThreads, 2)
       if (o < rows) {
         // up to 16 partials in flight, added in slot order
         const float* pr = part + size_t(m * rows + o) * g.PS;
-        for (int s0 = l; s0 < g.NS; s0 += 16 * g.tpr) {
-          float t[16];
+        int s0 = l;
+        for (; s0 + 3 * g.tpr < g.NS; s0 += 4 * g.tpr) {
+          float t[4];
 #pragma unroll
-          for (int k = 0; k < 16; ++k) t[k] = s0 + k * g.tpr < g.NS ? pr[s0 + k * g.tpr] : 0.f;
+          for (int k = 0; k < 4; ++k) t[k] = pr[s0 + k * g.tpr];
 #pragma unroll
-          for (int k = 0; k < 16; ++k) a += t[k];
+          for (int k = 0; k < 4; ++k) a += t[k];
         }
+        for (; s0 < g.NS; s0 += g.tpr) a += pr[s0];
       }
       for (int off = g.tpr >> 1; off > 0; off >>= 1) a += __shfl_xor_sync(0xffffffffu, a, off);
       const float b = NM == 2 ? __shfl_down_sync(0xffffffffu, a, g.tpr) : 0.f;  // the up row's sum

@@ -311,8 +311,12 @@ def run_gemv_tq2(B, w, d, x, xd):
 
 
 @pytest.mark.parametrize("xd", ["f32", "bf16"])
-@pytest.mark.parametrize("N,K", [(1, 256), (5, 512), (31, 5120), (33, 5120), (70, 1792), (130, 256)])
+@pytest.mark.parametrize("N,K", [(1, 256), (5, 512), (31, 5120), (33, 5120), (70, 1792), (130, 256),
+                                 (333, 768), (1000, 2560), (3, 22528)])
 def test_gemv_tq2_0_small(B, xd, N, K):
+    """Odd blocks 2 bytes past a 4-byte boundary, a tensor whose size is not
+    a multiple of 16 bytes (333 x 768), a partial last tile, the longest row
+    fp32 x supports (22528)."""
     g = rng(3 * N + K)
     w = ternary(g, N, K)
     d = synth.abs_normal_fp16_bits(g, (N, K // 256), 0.02)
@@ -320,6 +324,36 @@ def test_gemv_tq2_0_small(B, xd, N, K):
     x = rand_x(g, K, xd)
     y, ref, cond = run_gemv_tq2(B, w, d, x, xd)
     assert_close(y, ref, cond, TOL_F32, "gemv_tq2_0 %dx%d %s" % (N, K, xd))
+
+
+@pytest.mark.parametrize("xd", ["f32", "bf16"])
+def test_gemv_tq2_0_unaligned_x(B, xd):
+    """x one element past a 16-byte boundary (only element alignment is required)."""
+    g = rng(777)
+    N, K = 90, 1024
+    w = ternary(g, N, K)
+    d = synth.abs_normal_fp16_bits(g, (N, K // 256), 0.02)
+    x = rand_x(g, K + 1, xd)
+    xt = x_gpu(x, xd)[1:]
+    y = B.bl_gemv_tq2_0(B.bl_pack_tq2_0(to_gpu(w), fp16_gpu(d)), xt, N, K).cpu().numpy().astype(np.float64)
+    ref, cond = O.gemv_tq2_0(O.pack_tq2_0(w, d), x_f64(x[1:], xd), N, K)
+    assert_close(y, ref, cond, TOL_F32, "gemv_tq2_0 unaligned x %s" % xd)
+
+
+def test_gemv_tq2_0_many_rows(B):
+    """30400 x 4096: 200 rows per SM, 25 eight-row tiles through each CTA's
+    ring; sampled rows include the first and last of every 200-row share."""
+    g = rng(9090)
+    N, K = 30400, 4096
+    w = ternary(g, N, K)
+    d = synth.abs_normal_fp16_bits(g, (N, K // 256), 0.02)
+    x = rand_x(g, K, "bf16")
+    packed = B.bl_pack_tq2_0(to_gpu(w), fp16_gpu(d))
+    y = B.bl_gemv_tq2_0(packed, x_gpu(x, "bf16"), N, K).cpu().numpy().astype(np.float64)
+    edges = np.concatenate([np.arange(0, N, 200), np.arange(199, N, 200)])
+    rows = np.unique(np.concatenate([edges, g.choice(N, 2000, replace=False)]))
+    ref, cond = O.gemv_tq2_0(O.pack_tq2_0(w, d), x_f64(x, "bf16"), N, K, rows=rows)
+    assert_close(y[rows], ref, cond, TOL_F32, "tq2_0 30400x4096")
 
 
 def test_gemv_tq2_0_workload(B):
