@@ -177,7 +177,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int o = ob + lane / per_out;
         float a = 0.f;
         if (o < nr)
-          for (int s0 = l; s0 < g.nG; s0 += per_out) a += pb[o * g.PS + s0];
+        {
+          const float* pr = pb + o * g.PS;
+          int s0 = l;
+          for (; s0 + 3 * per_out < g.nG; s0 += 4 * per_out) {
+            const float t0 = pr[s0], t1 = pr[s0 + per_out], t2 = pr[s0 + 2 * per_out], t3 = pr[s0 + 3 * per_out];
+            a += t0; a += t1; a += t2; a += t3;
+          }
+          for (; s0 < g.nG; s0 += per_out) a += pr[s0];
+        }
         for (int off = per_out >> 1; off > 0; off >>= 1) a += __shfl_xor_sync(0xffffffffu, a, off);
         if (o < nr && l == 0) {
           float val = a * scale;
