@@ -43,6 +43,7 @@ struct Geom {
   int N, K, nG;         // rows, columns, groups per row (= slots)
   int nl, RT, PS, tpr;  // threads per slot, rows per tile, partials per row (odd), threads per row in the sums
   int ntiles, stages;
+  int one;              // 1 (a runtime value)
   uint32_t rb, sb;      // bit bytes and scale bytes of a row
   uint32_t stage_bytes, off_bar, off_stage, off_part, off_rec, off_q, smem;
   unsigned int* err;
@@ -126,6 +127,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // ---- this thread's slot ------------------------------------------------------
   const int slot = tid % g.nG, j0 = tid / g.nG;
+  // 2^(7-j) as runtime values, so that the class combine stays multiply-adds
+  int p2[7];
+#pragma unroll
+  for (int jc = 0; jc < 7; ++jc) p2[jc] = g.one << (7 - jc);
   const bool has_slot = tid < g.nG * g.nl;
   uint32_t xa[32];
   int qsum = 0;
@@ -159,10 +164,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int w = 0; w < 4; ++w)
 #pragma unroll
           for (int jc = 0; jc < 8; ++jc) acc[jc] = dp4a_us(wd[w] & (0x01010101u << jc), xa[8 * w + jc], acc[jc]);
-        int S = 0;
+        // acc_j = 2^j S_j, so T = sum_j acc_j 2^(7-j) = 2^7 sum_j S_j (|T| < 2^21)
+        int T = acc[7];
 #pragma unroll
-        for (int jc = 0; jc < 8; ++jc) S += acc[jc] >> jc;
-        const int dot = 2 * S - qsum;
+        for (int jc = 6; jc >= 0; --jc) T += acc[jc] * p2[jc];
+        const int dot = (T >> 6) - qsum;
         if (DOTS) dots[int64_t(r0 + row) * g.nG + slot] = dot;
         const float wsf = __half2float(__ushort_as_half(
             *reinterpret_cast<const uint16_t*>(stage + size_t(g.RT) * g.rb + size_t(row) * g.sb + 2 * slot)));
@@ -218,6 +224,7 @@ bool plan(Geom& g, int64_t N, int64_t K, int max_smem, int nsm) {
   g.tpr = 32;
   while (g.tpr > 1 && ((kThreads / g.tpr) < g.RT || g.tpr > g.nG)) g.tpr >>= 1;
   g.ntiles = int((N + g.RT - 1) / g.RT);
+  g.one = 1;
   g.stage_bytes = uint32_t(up(uint64_t(g.RT) * (g.rb + g.sb), 128));
   for (int st = 4; st >= 2; --st) {
     uint64_t off = 0;
