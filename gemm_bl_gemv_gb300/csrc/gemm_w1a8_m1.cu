@@ -44,6 +44,7 @@ struct Geom {
   int nl, RT, PS, tpr;  // threads per slot, rows per tile, partials per row (odd), threads per row in the sums
   int ntiles, stages;
   int one;              // 1 (a runtime value)
+  int rw;               // 1: the last warp has no slot and sums the rows (one tile behind)
   uint32_t rb, sb;      // bit bytes and scale bytes of a row
   uint32_t stage_bytes, off_bar, off_stage, off_part, off_rec, off_q, smem;
   unsigned int* err;
@@ -145,60 +146,86 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   const int per_out = g.tpr, opw = 32 / per_out, l = lane % per_out;
-  for (int i = 0; i < my_tiles; ++i) {
-    const int st = i % g.stages, t = t_begin + i;
-    const int r0 = t * g.RT, nr = min(g.RT, g.N - r0);
-    float* pb = part + size_t(i & 1) * g.RT * g.PS;
-    if (!abort_flag && !mbar_wait_bounded(&full[st], uint32_t(i / g.stages) & 1u, g.err)) abort_flag = 1;
-    const uint8_t* stage = smem + g.off_stage + size_t(st) * g.stage_bytes;
-    if (has_slot && !abort_flag && j0 < nr) {
-      // the next row's bit words are loaded while this row's are decoded
-      uint4 wn = *reinterpret_cast<const uint4*>(stage + size_t(j0) * g.rb + 16 * slot);
+  const bool rwarp = g.rw && warp == kWarps - 1;  // this warp sums rows while the others compute
+  for (int i = 0; i <= my_tiles; ++i) {
+    if (i < my_tiles && !rwarp) {
+      const int st = i % g.stages, t = t_begin + i;
+      const int r0 = t * g.RT, nr = min(g.RT, g.N - r0);
+      float* pb = part + size_t(i & 1) * g.RT * g.PS;
+      if (!abort_flag && !mbar_wait_bounded(&full[st], uint32_t(i / g.stages) & 1u, g.err)) abort_flag = 1;
+      const uint8_t* stage = smem + g.off_stage + size_t(st) * g.stage_bytes;
+      if (has_slot && !abort_flag && j0 < nr) {
+        // the next row's bit words are loaded while this row's are decoded
+        uint4 wn = *reinterpret_cast<const uint4*>(stage + size_t(j0) * g.rb + 16 * slot);
 #pragma unroll 1
-      for (int row = j0; row < nr; row += g.nl) {
-        const uint4 wv = wn;
-        if (row + g.nl < nr) wn = *reinterpret_cast<const uint4*>(stage + size_t(row + g.nl) * g.rb + 16 * slot);
-        const uint32_t wd[4] = {wv.x, wv.y, wv.z, wv.w};
-        int acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+        for (int row = j0; row < nr; row += g.nl) {
+          const uint4 wv = wn;
+          if (row + g.nl < nr) wn = *reinterpret_cast<const uint4*>(stage + size_t(row + g.nl) * g.rb + 16 * slot);
+          const uint32_t wd[4] = {wv.x, wv.y, wv.z, wv.w};
+          int acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
 #pragma unroll
-        for (int w = 0; w < 4; ++w)
+          for (int w = 0; w < 4; ++w)
 #pragma unroll
-          for (int jc = 0; jc < 8; ++jc) acc[jc] = dp4a_us(wd[w] & (0x01010101u << jc), xa[8 * w + jc], acc[jc]);
-        // acc_j = 2^j S_j, so T = sum_j acc_j 2^(7-j) = 2^7 sum_j S_j (|T| < 2^21)
-        int T = acc[7];
+            for (int jc = 0; jc < 8; ++jc) acc[jc] = dp4a_us(wd[w] & (0x01010101u << jc), xa[8 * w + jc], acc[jc]);
+          // acc_j = 2^j S_j, so T = sum_j acc_j 2^(7-j) = 2^7 sum_j S_j (|T| < 2^21)
+          int T = acc[7];
 #pragma unroll
-        for (int jc = 6; jc >= 0; --jc) T += acc[jc] * p2[jc];
-        const int dot = (T >> 6) - qsum;
-        if (DOTS) dots[int64_t(r0 + row) * g.nG + slot] = dot;
-        const float wsf = __half2float(__ushort_as_half(
-            *reinterpret_cast<const uint16_t*>(stage + size_t(g.RT) * g.rb + size_t(row) * g.sb + 2 * slot)));
-        pb[row * g.PS + slot] = wsf * float(dot);
+          for (int jc = 6; jc >= 0; --jc) T += acc[jc] * p2[jc];
+          const int dot = (T >> 6) - qsum;
+          if (DOTS) dots[int64_t(r0 + row) * g.nG + slot] = dot;
+          const float wsf = __half2float(__ushort_as_half(
+              *reinterpret_cast<const uint16_t*>(stage + size_t(g.RT) * g.rb + size_t(row) * g.sb + 2 * slot)));
+          pb[row * g.PS + slot] = wsf * float(dot);
+        }
       }
     }
-    __syncthreads();  // the tile's partials are complete and its stage is free
-    if (tid == 0 && i + g.stages < my_tiles && !abort_flag) issue(issued++);
-    // the tile's rows: tpr threads per row over the slots in order, then a butterfly
-    if (!abort_flag)
-      for (int ob = warp * opw; ob < nr; ob += kWarps * opw) {
-        const int o = ob + lane / per_out;
+    if (rwarp && i >= 1 && !abort_flag) {  // the rows of tile i - 1, one lane per row, slots in order
+      const int k = i - 1, r0 = (t_begin + k) * g.RT, nr = min(g.RT, g.N - r0);
+      const float* pb = part + size_t(k & 1) * g.RT * g.PS;
+      for (int o = lane; o < nr; o += 32) {
+        const float* pr = pb + o * g.PS;
         float a = 0.f;
-        if (o < nr)
-        {
-          const float* pr = pb + o * g.PS;
-          int s0 = l;
-          for (; s0 + 3 * per_out < g.nG; s0 += 4 * per_out) {
-            const float t0 = pr[s0], t1 = pr[s0 + per_out], t2 = pr[s0 + 2 * per_out], t3 = pr[s0 + 3 * per_out];
-            a += t0; a += t1; a += t2; a += t3;
-          }
-          for (; s0 < g.nG; s0 += per_out) a += pr[s0];
+        int s0 = 0;
+        for (; s0 + 3 < g.nG; s0 += 4) {
+          const float t0 = pr[s0], t1 = pr[s0 + 1], t2 = pr[s0 + 2], t3 = pr[s0 + 3];
+          a += t0; a += t1; a += t2; a += t3;
         }
-        for (int off = per_out >> 1; off > 0; off >>= 1) a += __shfl_xor_sync(0xffffffffu, a, off);
-        if (o < nr && l == 0) {
-          float val = a * scale;
-          if (bias) val += bf16_bits_to_f32(bias[r0 + o]);
-          y[r0 + o] = f32_to_bf16_bits_rn(val);
-        }
+        for (; s0 < g.nG; ++s0) a += pr[s0];
+        float val = a * scale;
+        if (bias) val += bf16_bits_to_f32(bias[r0 + o]);
+        y[r0 + o] = f32_to_bf16_bits_rn(val);
       }
+    }
+    __syncthreads();  // tile i's partials are complete, its stage is free, tile i - 1's rows are summed
+    if (i < my_tiles) {
+      if (tid == 0 && i + g.stages < my_tiles && !abort_flag) issue(issued++);
+      if (!g.rw) {
+        const int t = t_begin + i, r0 = t * g.RT, nr = min(g.RT, g.N - r0);
+        const float* pb = part + size_t(i & 1) * g.RT * g.PS;
+        // the tile's rows: tpr threads per row over the slots in order, then a butterfly
+        if (!abort_flag)
+          for (int ob = warp * opw; ob < nr; ob += kWarps * opw) {
+            const int o = ob + lane / per_out;
+            float a = 0.f;
+            if (o < nr)
+            {
+              const float* pr = pb + o * g.PS;
+              int s0 = l;
+              for (; s0 + 3 * per_out < g.nG; s0 += 4 * per_out) {
+                const float t0 = pr[s0], t1 = pr[s0 + per_out], t2 = pr[s0 + 2 * per_out], t3 = pr[s0 + 3 * per_out];
+                a += t0; a += t1; a += t2; a += t3;
+              }
+              for (; s0 < g.nG; s0 += per_out) a += pr[s0];
+            }
+            for (int off = per_out >> 1; off > 0; off >>= 1) a += __shfl_xor_sync(0xffffffffu, a, off);
+            if (o < nr && l == 0) {
+              float val = a * scale;
+              if (bias) val += bf16_bits_to_f32(bias[r0 + o]);
+              y[r0 + o] = f32_to_bf16_bits_rn(val);
+            }
+          }
+      }
+    }
   }
   if (abort_flag && tid == 0) {
     // let copies still in flight land before the CTA exits
@@ -225,6 +252,7 @@ bool plan(Geom& g, int64_t N, int64_t K, int max_smem, int nsm) {
   while (g.tpr > 1 && ((kThreads / g.tpr) < g.RT || g.tpr > g.nG)) g.tpr >>= 1;
   g.ntiles = int((N + g.RT - 1) / g.RT);
   g.one = 1;
+  g.rw = g.nG * g.nl <= kThreads - 32 ? 1 : 0;
   g.stage_bytes = uint32_t(up(uint64_t(g.RT) * (g.rb + g.sb), 128));
   for (int st = 4; st >= 2; --st) {
     uint64_t off = 0;
