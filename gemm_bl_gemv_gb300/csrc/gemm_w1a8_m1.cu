@@ -37,7 +37,7 @@ namespace {
 constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
 constexpr int kRecWords = 36;  // 32 activation words, the group's sum of q, padding (16-byte records)
-constexpr int kRowsPerThread = 8;  // rows of a tile per thread
+constexpr int kRowsPerThread = 10;  // rows of a tile per thread
 
 struct Geom {
   int N, K, nG;         // rows, columns, groups per row (= slots)
