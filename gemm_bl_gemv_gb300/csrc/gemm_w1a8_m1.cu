@@ -11,16 +11,21 @@
 // and class the mask  word & (0x01010101 << j)  holds the bits of elements
 // j, j+8, j+16, j+24 (one per byte, times 2^j), so one dp4a adds 2^j times
 // their activations.  The eight class sums are kept apart and combined once
-// per row and group (sum_j acc_j >> j, exact: acc_j is a multiple of 2^j),
-// then scaled by the row's fp16 group scale and written as the row's partial.
-// The threads of a slot take rows j, j + nl, ... (nl threads per slot).
+// per row and group: acc_j = 2^j S_j, so T = sum_j acc_j 2^(7-j) = 2^7 sum_j
+// S_j exactly, by multiply-adds with runtime powers of two (they stay on the
+// FMA pipe; the ALU pipe carries the masks); then scaled by the row's fp16
+// group scale and written as the row's partial.  The threads of a slot take
+// rows j, j + nl, ... (nl threads per slot).
 //
 // Streaming.  A CTA takes a contiguous range of tiles of RT rows; a tile's
 // bits and group scales are contiguous in memory and arrive by two bulk
-// copies into a ring of stages.  After a tile's products the CTA meets once:
-// the stage goes back to the copy engine and the tile's rows are summed (tpr
-// threads per row over the slots in order, then a fixed butterfly) while the
-// next tile's products fill the other partials buffer.
+// copies into a ring of stages.  After a tile's products the CTA meets once,
+// and the stage goes back to the copy engine.  When a whole warp holds no
+// slot, that warp sums the rows of the previous tile (a lane per row, the
+// slots in order) while the others compute the current one; otherwise all
+// warps sum the tile's rows after the barrier (tpr threads per row over the
+// slots in order, then a fixed butterfly).  Either way the other partials
+// buffer takes the next tile's products.
 //
 // Fused activation quantization (XQ != 0): each CTA quantizes the token
 // itself with act_quant.cuh's binary32 steps, so codes and scale equal the
