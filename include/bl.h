@@ -268,7 +268,10 @@ bl_status bl_gemv_tq2_0(const uint8_t* packed, const void* x, bl_dtype xt, float
  *              dot products are written too (a separate, slower kernel
  *              variant meant for verification).
  * The fp32 sum over groups runs in an order of the library's choosing.
- * M <= 8 runs a CUDA-core kernel (exact int32 group dots, dp4a); M > 8 runs
+ * M <= 8 runs a CUDA-core kernel (exact int32 group dots, dp4a): for one
+ * token with group = 128 (K / 128 <= 512, N * K / 128 a multiple of 8) an
+ * activation-stationary kernel whose threads keep a group of the token in
+ * registers while the rows stream past, otherwise a row-tiled one; M > 8 runs
  * on the tensor cores with B = +-ws (exact fp16), every product exact and
  * the sum over K in fp32 (group_dots must then be NULL, and K % 128 == 0).
  * Requires M >= 1, K % 32 == 0, group % 32 == 0, K % group == 0, N >= 1;
