@@ -13,10 +13,10 @@
 // Activations.  After that wait, each 128-element group of x is turned, once
 // per CTA, into exact fixed-point integers X = rint(x * 2^F_g) with
 // 2^(8D-2) <= max|x_g| * 2^F_g < 2^(8D-1), stored as D byte digits (unsigned
-// low digits, signed top digit).  D = 2 for bf16 x and bf16 y, 3 for bf16 x
-// and fp32 y, 4 for fp32 x.  Values within 7, 15 or 7 binades of the group
-// maximum are exact; smaller ones carry an absolute error of at most
-// 2^-(8D-1) max|x_g|.  A warp converts two groups at a time (16 lanes, 8
+// low digits, signed top digit).  D = 2 for bf16 x and bf16 y, 3 otherwise:
+// bf16 values within 7 (D = 2) or 15 (D = 3) binades of the group maximum
+// are exact; every other value (fp32 values with their 24-bit significands
+// included) carries an absolute error of at most 2^-(8D-1) max|x_g|.  A warp converts two groups at a time (16 lanes, 8
 // elements each) and writes the digits in the order the dot products read
 // them.
 //
@@ -514,8 +514,8 @@ cudaError_t launch_gemv_i2s_slot(const uint8_t* packed, const void* x, bl_dtype 
   if (xb)
     return yb ? run_slot<2, true, true, 1>(packed, packed, x, y, N, K, s, residual, rms_w, eps)
               : run_slot<3, true, false, 1>(packed, packed, x, y, N, K, s, residual, rms_w, eps);
-  return yb ? run_slot<4, false, true, 1>(packed, packed, x, y, N, K, s, residual, rms_w, eps)
-            : run_slot<4, false, false, 1>(packed, packed, x, y, N, K, s, residual, rms_w, eps);
+  return yb ? run_slot<3, false, true, 1>(packed, packed, x, y, N, K, s, residual, rms_w, eps)
+            : run_slot<3, false, false, 1>(packed, packed, x, y, N, K, s, residual, rms_w, eps);
 }
 
 cudaError_t launch_gemv_i2s_gate_up_slot(const uint8_t* packed_gate, const uint8_t* packed_up, const void* x,
@@ -524,8 +524,8 @@ cudaError_t launch_gemv_i2s_gate_up_slot(const uint8_t* packed_gate, const uint8
   if (xb)
     return hb ? run_slot<2, true, true, 2>(packed_gate, packed_up, x, h, N, K, s, nullptr, nullptr, 0.f)
               : run_slot<3, true, false, 2>(packed_gate, packed_up, x, h, N, K, s, nullptr, nullptr, 0.f);
-  return hb ? run_slot<4, false, true, 2>(packed_gate, packed_up, x, h, N, K, s, nullptr, nullptr, 0.f)
-            : run_slot<4, false, false, 2>(packed_gate, packed_up, x, h, N, K, s, nullptr, nullptr, 0.f);
+  return hb ? run_slot<3, false, true, 2>(packed_gate, packed_up, x, h, N, K, s, nullptr, nullptr, 0.f)
+            : run_slot<3, false, false, 2>(packed_gate, packed_up, x, h, N, K, s, nullptr, nullptr, 0.f);
 }
 
 }  // namespace bl

@@ -185,17 +185,20 @@ bl_status bl_quantize_act_absmax_int8(const void* x, bl_dtype xt, int64_t M, int
  *   x      : [K] fp32 (xt = BL_F32) or bf16 (xt = BL_BF16).
  *   y      : [N] fp32 or bf16 (yt).  bf16 output is rounded to nearest even.
  * Accuracy: within each 128-element group x is carried as a fixed-point
- * integer of 30 bits (fp32 input), 22 bits (bf16 input, fp32 output) or 14
- * bits (bf16 input and output) relative to the group's max|x|: values
- * within 7, 15 or 7 binades of the group maximum (respectively) are carried
- * exactly, smaller values with an absolute error of at most 2^-31, 2^-23 or
- * 2^-15 times the group maximum.  Products and sums inside a group are exact
+ * integer of 22 bits below the group maximum's leading bit (fp32 input, or
+ * bf16 input with fp32 output) or 14 bits (bf16 input and output); shapes
+ * the tiled fallback kernel takes (a CTA's rows, records and partials do
+ * not fit its shared memory, or x is not 16-byte aligned) carry fp32 input
+ * in 30 bits.  bf16 values within 15 (22 bits) or 7 (14 bits) binades of the
+ * group maximum are carried exactly; every other value, fp32 values
+ * included, with an absolute error of at most 2^-23, 2^-15 (or, 30 bits,
+ * 2^-31) times the group maximum.  Products and sums inside a group are exact
  * integers; the partial sums are converted to fp32 once each and added in
  * fp32, then rounded to bf16 if asked.  The error of y[i] is at most
  * rho |y[i]| + 1e-5 |scale| sum_j |w[i,j]| |x[j]| (rho = 1e-5 for fp32 output,
  * 2^-7 for bf16 output: twice its rounding), plus, for activations outside
  * the exact range, |scale| sum_g E max|x_g| sum_{j in g} |w[i,j]| with
- * E = 2^-31, 2^-23 or 2^-15 as above.
+ * E = 2^-23, 2^-15 or 2^-31 as above.
  * Requires K % 128 == 0, K <= 32768, N >= 1; `packed` 16-byte aligned; x
  * and y aligned to their element size.  Non-finite x gives unspecified y.
  */

@@ -83,7 +83,7 @@ def fixed_point_bound(w, x, scale, D, G=128):
     integer with 8D - 1 magnitude bits relative to the group's max|x|, so an
     element's absolute error is at most 2^-(8D-1) times that maximum.  Per
     output: |scale| * sum_g 2^-(8D-1) max|x_g| * sum_{k in g} |w[n,k]|.
-    D = 4 for fp32 x, 3 for bf16 x with fp32 y, 2 for bf16 x and y."""
+    D = 2 for bf16 x and y, 3 otherwise (4 for fp32 x on the tiled fallback)."""
     w = np.asarray(w)
     N, K = w.shape
     gmax = np.abs(np.asarray(x, np.float64)).reshape(K // G, G).max(axis=1)
