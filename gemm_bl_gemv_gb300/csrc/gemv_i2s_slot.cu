@@ -38,7 +38,10 @@
 // slot take every nl-th row (nl = threads per slot), so every thread does
 // the same work to within one row.  Finally one warp per output adds a
 // row's partials in slot order (lanes in fixed strides, then a fixed
-// butterfly), so results do not depend on timing.
+// butterfly), so results do not depend on timing.  For the fused gate/up,
+// when a whole warp holds no slot, the gate and up rows of the first half of
+// the outputs are computed first and that warp sums those outputs (a lane
+// per output, slots in order) while the other warps compute the rest.
 #include <algorithm>
 
 #include "bl_device.cuh"
@@ -72,6 +75,7 @@ struct SGeom {
   int RS;             // bytes per row in shared memory (this CTA's share: 32 nC)
   int PS;             // partials per row in shared memory (NS rounded up to odd: conflict-free row reads)
   int tpr;            // threads adding one row's partials (a power of two <= 32 / NM)
+  int ovl;            // NM == 2 and a whole warp holds no slot: the last warp sums half of the outputs early
   uint32_t off_rec, off_part, off_sum, smem;
   unsigned int* err;
   unsigned long long wait_ns;  // pipeline wait limit (0: the default; a test limit otherwise)
@@ -199,6 +203,14 @@ __device__ __forceinline__ float slot_dot(const uint32_t (&wd)[Slot<D>::W], cons
   return (p * fa) * fb;
 }
 
+// named barrier 1: arrive without waiting / wait for n threads in all
+__device__ __forceinline__ void named_arrive(int id, int n) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+__device__ __forceinline__ void named_sync(int id, int n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
 template <bool YB>
 __device__ __forceinline__ void store_out(void* y, int row, float v) {
   if (YB)
@@ -304,40 +316,116 @@ __global__ void __launch_bounds__(kThreads, 2)
 
   // ---- slot dot products -------------------------------------------------------
   bool waited = false;
-  // consecutive threads take consecutive slots of the same rows (one 16-byte
-  // row load per thread, a warp's loads contiguous); the nl threads of a slot
-  // take rows j, j + nl, ...
-  for (int vs = tid; vs < g.NS * g.nl; vs += kThreads) {
-    const int s = vs % g.NS, j = vs / g.NS;
-    uint32_t xd[C::kDig];
-    const uint32_t* r = rec + size_t(s) * C::kStride;
+  // With g.ovl (fused gate/up, a whole warp without a slot) the rows of the
+  // first h1 outputs -- gate rows [0, h1) and up rows [rows, rows + h1) --
+  // come first; the last warp waits for them at a named barrier and sums
+  // those outputs while the other warps compute the remaining rows.
+  const int h1 = (NM == 2 && g.ovl) ? rows / 2 : 0;
+  if (h1 > 0) {
+    if (warp < kWarps - 1) {
+      const bool has = tid < g.NS * g.nl;  // one slot at most (NS * nl <= 480)
+      const int s = tid % g.NS, j = tid / g.NS;
+      uint32_t xd[C::kDig];
+      int S[D];
+      float fa = 0.f, fb = 0.f;
+      if (has) {
+        const uint32_t* r = rec + size_t(s) * C::kStride;
 #pragma unroll
-    for (int k = 0; k < C::kDig / 4; ++k) {
-      const uint4 q = *reinterpret_cast<const uint4*>(r + 4 * k);
-      xd[4 * k] = q.x; xd[4 * k + 1] = q.y; xd[4 * k + 2] = q.z; xd[4 * k + 3] = q.w;
-    }
-    int S[D];
+        for (int k = 0; k < C::kDig / 4; ++k) {
+          const uint4 q = *reinterpret_cast<const uint4*>(r + 4 * k);
+          xd[4 * k] = q.x; xd[4 * k + 1] = q.y; xd[4 * k + 2] = q.z; xd[4 * k + 3] = q.w;
+        }
 #pragma unroll
-    for (int d = 0; d < D; ++d) S[d] = reinterpret_cast<const int*>(r + C::kDig)[d];
-    const float fa = reinterpret_cast<const float*>(r + C::kDig)[D];
-    const float fb = reinterpret_cast<const float*>(r + C::kDig)[D + 1];
-    if (!waited) {
-      waited = true;
-      if (!abort_flag && !mbar_wait_limited(&wbar, 0, g.err, g.wait_ns)) abort_flag = 1;
-    }
-    if (abort_flag) break;
-    const uint8_t* wp = smem + size_t(s) * (4 * C::W);
-#pragma unroll 1
-    for (int row = j; row < R; row += g.nl) {
-      uint32_t wd[C::W];
-      if constexpr (C::W == 4) {
-        const uint4 q = *reinterpret_cast<const uint4*>(wp + size_t(row) * g.RS);
-        wd[0] = q.x; wd[1] = q.y; wd[2] = q.z; wd[3] = q.w;
-      } else {
-        const uint2 q = *reinterpret_cast<const uint2*>(wp + size_t(row) * g.RS);
-        wd[0] = q.x; wd[1] = q.y;
+        for (int d = 0; d < D; ++d) S[d] = reinterpret_cast<const int*>(r + C::kDig)[d];
+        fa = reinterpret_cast<const float*>(r + C::kDig)[D];
+        fb = reinterpret_cast<const float*>(r + C::kDig)[D + 1];
+        if (!abort_flag && !mbar_wait_limited(&wbar, 0, g.err, g.wait_ns)) abort_flag = 1;
       }
-      part[size_t(row) * g.PS + s] = slot_dot<D>(wd, xd, S, fa, fb);
+      const bool go = has && !abort_flag;
+      const uint8_t* wp = smem + size_t(s) * (4 * C::W);
+      auto do_row = [&](int row) {
+        uint32_t wd[C::W];
+        if constexpr (C::W == 4) {
+          const uint4 q = *reinterpret_cast<const uint4*>(wp + size_t(row) * g.RS);
+          wd[0] = q.x; wd[1] = q.y; wd[2] = q.z; wd[3] = q.w;
+        } else {
+          const uint2 q = *reinterpret_cast<const uint2*>(wp + size_t(row) * g.RS);
+          wd[0] = q.x; wd[1] = q.y;
+        }
+        part[size_t(row) * g.PS + s] = slot_dot<D>(wd, xd, S, fa, fb);
+      };
+      const int hh = rows - h1;
+      int v = j;  // processing order: gate/up rows of outputs [0, h1), then of [h1, rows)
+      if (go) {
+#pragma unroll 1
+        for (; v < 2 * h1; v += g.nl) do_row(v < h1 ? v : rows + (v - h1));
+      }
+      named_arrive(1, kThreads);  // every thread of warps 0 .. kWarps-2, on every path
+      if (go) {
+#pragma unroll 1
+        for (; v < R; v += g.nl) {
+          const int u = v - 2 * h1;
+          do_row(u < hh ? h1 + u : rows + h1 + (u - hh));
+        }
+      }
+    } else {
+      named_sync(1, kThreads);
+      if constexpr (NM == 2) {
+        if (!abort_flag) {
+          for (int o = lane; o < h1; o += 32) {
+            const float* pg = part + size_t(o) * g.PS;
+            const float* pu = part + size_t(rows + o) * g.PS;
+            float a = 0.f, b = 0.f;
+            int s0 = 0;
+            for (; s0 + 3 < g.NS; s0 += 4) {
+              const float t0 = pg[s0], t1 = pg[s0 + 1], t2 = pg[s0 + 2], t3 = pg[s0 + 3];
+              const float u0 = pu[s0], u1 = pu[s0 + 1], u2 = pu[s0 + 2], u3 = pu[s0 + 3];
+              a += t0; a += t1; a += t2; a += t3;
+              b += u0; b += u1; b += u2; b += u3;
+            }
+            for (; s0 < g.NS; ++s0) {
+              a += pg[s0];
+              b += pu[s0];
+            }
+            const float gv = fmaxf(a * sc0, 0.f), uv = b * sc1;
+            store_out<YB>(y, r0 + o, (gv * gv) * uv);
+          }
+        }
+      }
+    }
+  } else {
+    for (int vs = tid; vs < g.NS * g.nl; vs += kThreads) {
+      const int s = vs % g.NS, j = vs / g.NS;
+      uint32_t xd[C::kDig];
+      const uint32_t* r = rec + size_t(s) * C::kStride;
+#pragma unroll
+      for (int k = 0; k < C::kDig / 4; ++k) {
+        const uint4 q = *reinterpret_cast<const uint4*>(r + 4 * k);
+        xd[4 * k] = q.x; xd[4 * k + 1] = q.y; xd[4 * k + 2] = q.z; xd[4 * k + 3] = q.w;
+      }
+      int S[D];
+#pragma unroll
+      for (int d = 0; d < D; ++d) S[d] = reinterpret_cast<const int*>(r + C::kDig)[d];
+      const float fa = reinterpret_cast<const float*>(r + C::kDig)[D];
+      const float fb = reinterpret_cast<const float*>(r + C::kDig)[D + 1];
+      if (!waited) {
+        waited = true;
+        if (!abort_flag && !mbar_wait_limited(&wbar, 0, g.err, g.wait_ns)) abort_flag = 1;
+      }
+      if (abort_flag) break;
+      const uint8_t* wp = smem + size_t(s) * (4 * C::W);
+#pragma unroll 1
+      for (int row = j; row < R; row += g.nl) {
+        uint32_t wd[C::W];
+        if constexpr (C::W == 4) {
+          const uint4 q = *reinterpret_cast<const uint4*>(wp + size_t(row) * g.RS);
+          wd[0] = q.x; wd[1] = q.y; wd[2] = q.z; wd[3] = q.w;
+        } else {
+          const uint2 q = *reinterpret_cast<const uint2*>(wp + size_t(row) * g.RS);
+          wd[0] = q.x; wd[1] = q.y;
+        }
+        part[size_t(row) * g.PS + s] = slot_dot<D>(wd, xd, S, fa, fb);
+      }
     }
   }
   __syncthreads();
@@ -349,7 +437,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int per_out = NM * g.tpr;         // threads per output
     const int opw = 32 / per_out;           // outputs per warp and pass
     const int sub = lane % per_out, m = sub / g.tpr, l = sub % g.tpr;
-    for (int ob = warp * opw; ob < rows; ob += kWarps * opw) {
+    for (int ob = h1 + warp * opw; ob < rows; ob += kWarps * opw) {
       const int o = ob + lane / per_out;
       float a = 0.f;
       if (o < rows) {
@@ -429,6 +517,7 @@ bool plan_slot(SGeom& g, int64_t N, int64_t K, int max_smem, int nsm, int ks) {
   g.RS = 32 * g.nC;
   const int rows_max = g.q + (g.rem ? 1 : 0);
   // threads per row for the final sums: as many as fit one pass over the rows, at most NS
+  g.ovl = (NM == 2 && g.NS * g.nl <= kThreads - 32 && rows_max >= 2) ? 1 : 0;
   g.tpr = 32 / NM;
   while (g.tpr > 1 && ((kThreads / (NM * g.tpr)) < rows_max || g.tpr > g.NS)) g.tpr >>= 1;
   const uint64_t R = uint64_t(NM) * rows_max;
