@@ -240,7 +240,23 @@ __global__ void __launch_bounds__((MT == 1 ? 512 : 256), (MT >= 2 && MT <= 4 ? 2
         for (int j = 0; j < 8; ++j) {
           uint32_t qj[MT];  // activation words of class j, one per token (broadcast reads)
 #pragma unroll
-          for (int m = 0; m < MT; ++m) qj[m] = MT == 1 ? q8[j] : qw[j * MT + m];
+          for (int m = 0; m < MT; ++m) qj[m] = MT == 1 ? q8[j] : 0u;
+          if constexpr (MT > 1 && MT % 4 == 0) {
+#pragma unroll
+            for (int m4 = 0; m4 < MT; m4 += 4) {
+              const uint4 v4 = *reinterpret_cast<const uint4*>(qw + j * MT + m4);
+              qj[m4] = v4.x; qj[m4 + 1] = v4.y; qj[m4 + 2] = v4.z; qj[m4 + 3] = v4.w;
+            }
+          } else if constexpr (MT > 1 && MT % 2 == 0) {
+#pragma unroll
+            for (int m2 = 0; m2 < MT; m2 += 2) {
+              const uint2 v2 = *reinterpret_cast<const uint2*>(qw + j * MT + m2);
+              qj[m2] = v2.x; qj[m2 + 1] = v2.y;
+            }
+          } else if constexpr (MT > 1) {
+#pragma unroll
+            for (int m = 0; m < MT; ++m) qj[m] = qw[j * MT + m];
+          }
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
             if (MT == 1) {
@@ -359,7 +375,8 @@ bool plan(Geom& g, int M, int64_t N, int64_t K, int G, int max_smem, int nsm) {
   while (slot % 128 != 32) slot += 16;
   g.slot = slot;
   g.stage_bytes = uint32_t(up(uint64_t(kRows) * slot, 128));
-  g.rec_words = int(up(uint64_t(g.wpc) * 8 * M + M, 4));  // 16-byte records
+  g.rec_words = int(up(uint64_t(g.wpc) * 8 * M + M, 4));  // 16-byte records,
+  if ((g.rec_words / 4) % 2 == 0) g.rec_words += 4;          // an odd number of 16-byte units apart
   const int warps = g.wk * g.wr;
   const int64_t tiles_per_warp = (g.ntiles + int64_t(g.wr) * nsm - 1) / (int64_t(g.wr) * nsm);
   for (int st = int(std::min<int64_t>(4, std::max<int64_t>(1, tiles_per_warp))); st >= 1; --st) {
